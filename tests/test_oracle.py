@@ -1,0 +1,247 @@
+"""Pins for the fp64 oracle against things other than itself (CPU only).
+
+Each test targets a mistake the oracle could plausibly contain: a dropped
+centring term, a wrong sign, a transposed Sigma, a wrong GQA head mapping, an
+off-by-one in the causal window, or a bad softmax normaliser.
+
+Definition pinned (page "Parallax: parametrized local linear attention for
+language modeling", section "Core mechanism", output equation):
+o_i = o^SA_i - Sigma_KV^(i) rho_i, with Sigma_KV^(i) the softmax-weighted,
+centred KV cross-covariance of the keys query i sees.
+"""
+import glob
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from parametrized_local_linear_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _parse_fixture(path):
+    rec = {"k": [], "v": []}
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            vals = [float(x) for x in vals]
+            if key in ("k", "v"):
+                rec[key].append(vals)
+            else:
+                rec[key] = vals
+    return rec
+
+
+@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(GOLDEN, "hand_*.txt"))))
+def test_hand_worked_examples(path):
+    rec = _parse_fixture(path)
+    d = len(rec["q"])
+    o, lse, sig = oracle.query(np.array(rec["q"]), np.array(rec["rho"]), np.array(rec["k"]),
+                               np.array(rec["v"]), tau=rec["tau"][0], with_sigma=True)
+    np.testing.assert_allclose(o, rec["out"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, rec["lse"][0], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sig.reshape(-1), rec["sigma"], rtol=0, atol=1e-12)
+    assert sig.shape == (d, d)
+
+
+def _small(B=2, Hq=4, Hkv=2, L=24, d=8, seed=3, r_std=0.3):
+    return inputs.prefill_inputs(B, Hq, Hkv, L, d, torch.float64, r_std, seed)
+
+
+def test_row0_closed_form():
+    """Row 0 sees one key: weight 1, Sigma = 0, so o = v_0 whatever rho is."""
+    q, k, v, r = _small()
+    out, lse = oracle.prefill(q, k, v, r)
+    G = q.shape[1] // k.shape[1]
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            np.testing.assert_allclose(out[b, h, 0], v[b, h // G, 0].numpy(), rtol=0, atol=1e-14)
+            s0 = float(q[b, h, 0] @ k[b, h // G, 0]) / math.sqrt(q.shape[-1])
+            assert abs(lse[b, h, 0] - s0) < 1e-12
+
+
+def test_row1_closed_form():
+    """Row 1 sees two keys: Sigma = w0 w1 (v1 - v0)(k1 - k0)^T."""
+    q, k, v, r = _small(seed=11)
+    out, _ = oracle.prefill(q, k, v, r)
+    d = q.shape[-1]
+    G = q.shape[1] // k.shape[1]
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            K = k[b, h // G, :2].numpy(); V = v[b, h // G, :2].numpy()
+            qi = q[b, h, 1].numpy(); ri = r[b, h, 1].numpy()
+            s = K @ qi / math.sqrt(d)
+            w1 = 1.0 / (1.0 + math.exp(s[0] - s[1])); w0 = 1.0 - w1
+            osa = w0 * V[0] + w1 * V[1]
+            want = osa - w0 * w1 * (V[1] - V[0]) * float((K[1] - K[0]) @ ri)
+            np.testing.assert_allclose(out[b, h, 1], want, rtol=0, atol=1e-12)
+
+
+def test_rho_zero_is_softmax_attention():
+    """W_R = 0 (rho = 0) reduces Parallax to causal softmax attention: pinned to
+    torch's fp64 scaled_dot_product_attention with KV heads repeated for GQA."""
+    q, k, v, r = _small(B=2, Hq=6, Hkv=2, L=40, d=16, seed=5)
+    out, lse = oracle.prefill(q, k, v, torch.zeros_like(r))
+    G = q.shape[1] // k.shape[1]
+    kk = k.repeat_interleave(G, dim=1); vv = v.repeat_interleave(G, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=True)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=0, atol=1e-12)
+    L = q.shape[2]
+    scores = (q @ kk.transpose(-1, -2)) / math.sqrt(q.shape[-1])
+    mask = torch.ones(L, L, dtype=torch.bool).tril()
+    ref_lse = torch.logsumexp(scores.masked_fill(~mask, -math.inf), dim=-1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("n,d", [(1, 3), (5, 4), (37, 8), (200, 16)])
+def test_sigma_is_weighted_covariance(n, d):
+    """Sigma equals the V-K block of numpy's weighted (biased) covariance with
+    the softmax weights as analytic weights; softmax from scipy."""
+    rng = np.random.default_rng(n * 100 + d)
+    q = rng.normal(size=d); rho = rng.normal(size=d)
+    K = rng.normal(size=(n, d)); V = rng.normal(size=(n, d))
+    o, lse, sig = oracle.query(q, rho, K, V, with_sigma=True)
+    w = scipy.special.softmax(K @ q / math.sqrt(d))
+    if n == 1:
+        ref = np.zeros((d, d))
+    else:
+        ref = np.cov(np.vstack([V.T, K.T]), aweights=w, bias=True)[:d, d:]
+    np.testing.assert_allclose(sig, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o, w @ V - ref @ rho, rtol=0, atol=1e-12)
+    assert abs(lse - scipy.special.logsumexp(K @ q / math.sqrt(d))) < 1e-12
+
+
+def test_uniform_weights_give_population_covariance():
+    rng = np.random.default_rng(7)
+    n, d = 9, 5
+    K = rng.normal(size=(n, d)); V = rng.normal(size=(n, d)); rho = rng.normal(size=d)
+    _, _, sig = oracle.query(np.zeros(d), rho, K, V, with_sigma=True)
+    ref = np.cov(V.T, K.T, bias=True)[:d, d:]
+    np.testing.assert_allclose(sig, ref, rtol=0, atol=1e-13)
+
+
+def _dense_streaming_identity(q, k, v, r):
+    """o = O1 - O2 + O1*s from dense matrices: P = exp(S - rowmax) on the
+    causal window, O1 = P V / l, O2 = (P*T) V / l, s = rowsum(P*T) / l,
+    T = R K^T (unscaled)."""
+    B, Hq, L, d = q.shape
+    G = Hq // k.shape[1]
+    q = q.numpy(); r = r.numpy()
+    k = np.repeat(k.numpy(), G, axis=1); v = np.repeat(v.numpy(), G, axis=1)
+    S = q @ k.transpose(0, 1, 3, 2) / math.sqrt(d)
+    causal = np.tril(np.ones((L, L), dtype=bool))
+    S = np.where(causal, S, -np.inf)
+    P = np.exp(S - S.max(-1, keepdims=True))
+    ell = P.sum(-1, keepdims=True)
+    T = r @ k.transpose(0, 1, 3, 2)
+    PT = P * T
+    O1 = P @ v / ell
+    O2 = PT @ v / ell
+    s = PT.sum(-1, keepdims=True) / ell
+    return O1 - O2 + O1 * s
+
+
+@pytest.mark.parametrize("d,L,Hq,Hkv", [(4, 16, 2, 2), (8, 33, 4, 2), (64, 64, 4, 1)])
+def test_matches_dense_streaming_identity(d, L, Hq, Hkv):
+    q, k, v, r = _small(B=2, Hq=Hq, Hkv=Hkv, L=L, d=d, seed=d + L)
+    out, _ = oracle.prefill(q, k, v, r)
+    np.testing.assert_allclose(out, _dense_streaming_identity(q, k, v, r), rtol=0, atol=1e-11)
+
+
+def test_shift_v_shifts_output():
+    q, k, v, r = _small(seed=21)
+    c = torch.linspace(-2, 3, q.shape[-1], dtype=torch.float64)
+    o0, _ = oracle.prefill(q, k, v, r)
+    o1, _ = oracle.prefill(q, k, v + c, r)
+    np.testing.assert_allclose(o1, o0 + c.numpy(), rtol=0, atol=1e-11)
+
+
+def test_shift_k_leaves_output_unchanged():
+    """A common shift of every key changes each score by q.c (the same for every
+    key of a row), so the weights, o^SA and the centred Sigma do not move."""
+    q, k, v, r = _small(seed=22)
+    c = torch.linspace(1, -1, q.shape[-1], dtype=torch.float64)
+    o0, _ = oracle.prefill(q, k, v, r)
+    o1, _ = oracle.prefill(q, k + c, v, r)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-11)
+
+
+def test_uncentred_covariance_would_fail_the_k_shift_pin():
+    """The k-shift pin discriminates: an uncentred sum_j w_j v_j k_j^T does move."""
+    rng = np.random.default_rng(4)
+    n, d = 12, 6
+    q = rng.normal(size=d); rho = rng.normal(size=d)
+    K = rng.normal(size=(n, d)); V = rng.normal(size=(n, d)); c = np.full(d, 0.7)
+
+    def uncentred(K):
+        w = scipy.special.softmax(K @ q / math.sqrt(d))
+        return w @ V - (V.T * w) @ K @ rho
+
+    assert np.max(np.abs(uncentred(K + c) - uncentred(K))) > 1e-3
+    o0, _ = oracle.query(q, rho, K, V)
+    o1, _ = oracle.query(q, rho, K + c, V)
+    np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-12)
+
+
+def test_correction_is_linear_in_rho():
+    q, k, v, r = _small(seed=23)
+    r2 = _small(seed=24)[3]
+    base, _ = oracle.prefill(q, k, v, torch.zeros_like(r))
+    oa, _ = oracle.prefill(q, k, v, r)
+    ob, _ = oracle.prefill(q, k, v, r2)
+    oab, _ = oracle.prefill(q, k, v, 2.5 * r - 0.5 * r2)
+    np.testing.assert_allclose(oab - base, 2.5 * (oa - base) - 0.5 * (ob - base), rtol=0, atol=1e-11)
+
+
+def test_equal_keys_remove_the_correction():
+    """All keys equal: k_j - mu = 0, Sigma = 0, o = o^SA (uniform average of v)."""
+    q, k, v, r = _small(seed=25)
+    k = k[:, :, :1].expand_as(k).contiguous()
+    out, _ = oracle.prefill(q, k, v, r)
+    G = q.shape[1] // k.shape[1]
+    L = q.shape[2]
+    cum = torch.cumsum(v, dim=2) / torch.arange(1, L + 1, dtype=torch.float64)[:, None]
+    np.testing.assert_allclose(out, cum.repeat_interleave(G, dim=1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_decode_equals_last_prefill_row():
+    """A decode query over a packed ragged cache equals the last causal row of a
+    prefill over the same keys (checks the packed-offset walk)."""
+    Hq, Hkv, d = 4, 2, 8
+    lens = [5, 1, 17, 9]
+    q, r, kc, vc, sl = inputs.decode_inputs(len(lens), Hq, Hkv, d, lens, torch.float64, 0.3, 9)
+    out, lse = oracle.decode(q, r, kc, vc, sl)
+    off = 0
+    for b, n in enumerate(lens):
+        kb = kc[off:off + n].permute(1, 0, 2)[None]
+        vb = vc[off:off + n].permute(1, 0, 2)[None]
+        qb = torch.zeros(1, Hq, n, d, dtype=torch.float64); rb = torch.zeros_like(qb)
+        qb[0, :, -1] = q[b]; rb[0, :, -1] = r[b]
+        po, pl = oracle.prefill(qb, kb, vb, rb, rows=[(0, h, n - 1) for h in range(Hq)])
+        np.testing.assert_allclose(out[b], po, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[b], pl, rtol=0, atol=1e-13)
+        off += n
+
+
+def test_decode_empty_sequence_is_zero():
+    q, r, kc, vc, sl = inputs.decode_inputs(3, 2, 1, 4, [3, 0, 2], torch.float64, 0.3, 1)
+    out, lse = oracle.decode(q, r, kc, vc, sl)
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+    assert np.all(np.isfinite(out[[0, 2]]))
+
+
+def test_row_sampling_matches_full_pass():
+    q, k, v, r = _small(B=1, Hq=2, Hkv=1, L=30, d=8, seed=31)
+    full, flse = oracle.prefill(q, k, v, r)
+    rows = [(0, 1, 29), (0, 0, 0), (0, 1, 7)]
+    o, l = oracle.prefill(q, k, v, r, rows=rows)
+    for n, (b, h, i) in enumerate(rows):
+        assert np.array_equal(o[n], full[b, h, i]) and l[n] == flse[b, h, i]
