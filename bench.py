@@ -1,0 +1,407 @@
+"""Benchmark of the Parallax forward hot path on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+the causal prefill of the 0.6B-shaped workload (B=4, Hq=16, Hkv=8, L=4096,
+d=128, bf16) followed by a decode of the batched workload (B=64, Hq=16,
+Hkv=8, d=128, 8192 cached tokens each). ``value`` is the prefill throughput
+in algorithmic TFLOP/s (8 d flops per causal pair); the decode throughput in
+algorithmic HBM GB/s is the ``decode`` object. Both are timed per launch with
+CUDA events on the launching stream; inputs are resident in HBM and larger
+than L2, so no flush is needed between steps. The 1.7B-shaped prefill and
+the ragged long-context decode are timed after the steps (``extra``).
+
+``--impl reference`` times the fp64 CPU oracle instead (the only other
+implementation of this method here), on a bounded row sample per step.
+
+Under torchrun each rank runs the same per-rank workload on its own GPU
+(weak scaling, no collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from parametrized_local_linear_gb300 import inputs  # noqa: E402
+
+METRIC = "Parallax fwd: prefill TFLOP/s, decode HBM GB/s; % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu
+# summaries under profiles/ (None until captured for the current kernel).
+NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": None, "decode_split_kernel": None}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak(peaks, key):
+    v = peaks.get(key)
+    if isinstance(v, dict):
+        v = v.get("value")
+    return float(v) if v is not None else FALLBACK_PEAKS[key]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_prefill_sample(w, q, k, v, r, budget_s, seed, threads=None):
+    """Time the fp64 oracle on seeded random causal rows of workload w until
+    about budget_s seconds of oracle time; return (algorithmic flops of the
+    rows done, oracle seconds, rows, threads). Host copies are not timed."""
+    import random
+
+    import oracle
+    rng = random.Random(seed)
+    threads = oracle.default_threads() if threads is None else threads
+    done_flops, rows_done, secs = 0, 0, 0.0
+    while secs < budget_s:
+        b, h = rng.randrange(w.B), rng.randrange(w.Hq)
+        g = h // (w.Hq // w.Hkv)
+        rows = [(0, 0, rng.randrange(w.L)) for _ in range(threads)]
+        qs = q[b:b + 1, h:h + 1].cpu(); rs = r[b:b + 1, h:h + 1].cpu()
+        ks = k[b:b + 1, g:g + 1].cpu(); vs = v[b:b + 1, g:g + 1].cpu()
+        ts = time.perf_counter()
+        oracle.prefill(qs, ks, vs, rs, rows=rows, threads=threads)
+        secs += time.perf_counter() - ts
+        done_flops += sum(8 * w.d * (i + 1) for _, _, i in rows)
+        rows_done += len(rows)
+    return done_flops, secs, rows_done, threads
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step is a bounded row sample."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = inputs.PREFILL_0P6B
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    q, k, v, r = inputs.prefill_inputs_for(w, device=dev)
+    per_step = max(3.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_prefill_sample(w, q, k, v, r, 1.0, seed=7)
+    flops, secs, rows, threads = 0, 0.0, 0, 1
+    for s in range(args.steps):
+        f, t, n, threads = oracle_prefill_sample(w, q, k, v, r, per_step, seed=100 + s)
+        flops += f; secs += t; rows += n
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "oracle": "explicit Sigma_KV per query, fp64, C"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} random causal rows of {w.name}, "
+                                   f"~{per_step:.0f} s of CPU work per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="plx", choices=["plx", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the 1.7B / ragged timings")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    from parametrized_local_linear_gb300 import (build, plx_check_device_error, plx_decode_fwd,
+                                                 plx_prefill_fwd)
+    if rank == 0 or world == 1:
+        build.build()
+    barrier(world)
+    build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peaks_src = load_peaks()
+
+    wp, wd = inputs.PREFILL_0P6B, inputs.DECODE_B64
+    q, k, v, r = inputs.prefill_inputs_for(wp, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(wp.B, wp.Hq, wp.L, device=dev)
+    dq, dr, kc, vc, sl = inputs.decode_inputs_for(wd, device=dev)
+    sl = sl.to(dev)
+    dout = torch.empty_like(dq)
+    dbytes = wd.bytes_moved()
+
+    def step(ev):
+        ev[0].record(stream)
+        plx_prefill_fwd(q, k, v, r, out, lse)
+        ev[1].record(stream)
+        plx_decode_fwd(dq, dr, kc, vc, sl, dout)
+        ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize(dev)
+    plx_check_device_error()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let the sampler start
+        t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    plx_check_device_error()
+    pre_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+    total_ms = t0.elapsed_time(t1)
+    pre_ms_max = max_over_ranks(pre_ms, world, dev)
+    dec_ms_max = max_over_ranks(dec_ms, world, dev)
+    total_ms_max = max_over_ranks(total_ms, world, dev)
+    K = args.steps
+    value = world * wp.flops * K / (pre_ms_max * 1e-3) / 1e12
+    dec_gbs = world * dbytes * K / (dec_ms_max * 1e-3) / 1e9
+    pre_launch_s = pre_ms / K * 1e-3
+    dec_launch_s = dec_ms / K * 1e-3
+    tc_peak = _peak(peaks, "bf16_tflops")
+    hbm_peak = _peak(peaks, "hbm_gbs")
+
+    # ---------------------------------------------------------------- e2e
+    # Through the same C-ABI call, from pinned host buffers: H2D of q, k, v, r,
+    # the prefill, D2H of out (and the decode step likewise) inside the timing.
+    hq = [t.cpu().pin_memory() for t in (q, k, v, r)]
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hd = [t.cpu().pin_memory() for t in (dq, dr)]
+    hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hq + hd)
+    d2h = hout.numel() * hout.element_size() + hdout.numel() * hdout.element_size()
+
+    def e2e_step():
+        dq_ = [t.to(dev, non_blocking=True) for t in hq]
+        o_ = torch.empty_like(dq_[0])
+        plx_prefill_fwd(*dq_, o_)
+        hout.copy_(o_, non_blocking=True)
+        dd_ = [t.to(dev, non_blocking=True) for t in hd]
+        od_ = torch.empty_like(dd_[0])
+        plx_decode_fwd(dd_[0], dd_[1], kc, vc, sl, od_)
+        hdout.copy_(od_, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    ke = max(3, min(K, 10))
+    e0.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / ke
+    # The e2e step also contains the decode; count its time, credit only prefill flops.
+    e2e_value = world * wp.flops / (e2e_ms * 1e-3) / 1e12
+
+    # ---------------------------------------------------------------- extra
+    extra = {}
+    if not args.no_extra:
+        del hq, hd
+        w3 = inputs.PREFILL_1P7B
+        q3, k3, v3, r3 = inputs.prefill_inputs_for(w3, device=dev)
+        o3 = torch.empty_like(q3)
+        for _ in range(3):
+            plx_prefill_fwd(q3, k3, v3, r3, o3)
+        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+        n3 = 5
+        a.record(stream)
+        for _ in range(n3):
+            plx_prefill_fwd(q3, k3, v3, r3, o3)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        t3 = a.elapsed_time(b) / n3 * 1e-3
+        extra[w3.name] = {"value": w3.flops / t3 / 1e12, "unit": "TFLOP/s", "ms": t3 * 1e3,
+                          "frac_of_peak": w3.flops / t3 / 1e12 / tc_peak}
+        del q3, k3, v3, r3, o3
+        w5 = inputs.DECODE_RAGGED
+        d5 = inputs.decode_inputs_for(w5, device=dev)
+        sl5 = d5[4].to(dev)
+        o5 = torch.empty_like(d5[0])
+        for _ in range(3):
+            plx_decode_fwd(d5[0], d5[1], d5[2], d5[3], sl5, o5)
+        n5 = 10
+        a.record(stream)
+        for _ in range(n5):
+            plx_decode_fwd(d5[0], d5[1], d5[2], d5[3], sl5, o5)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        t5 = a.elapsed_time(b) / n5 * 1e-3
+        by5 = w5.bytes_moved()
+        extra[w5.name] = {"value": by5 / t5 / 1e9, "unit": "GB/s", "ms": t5 * 1e3,
+                          "bytes": by5, "seqlens": w5.seqlens().tolist(),
+                          "frac_of_peak": by5 / t5 / 1e9 / hbm_peak}
+        del d5
+        plx_check_device_error()
+
+    # ---------------------------------------------------------------- cpu baseline
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
+        import oracle
+        oracle.build()
+        f, secs, rows, threads = oracle_prefill_sample(wp, q, k, v, r, args.cpu_seconds, seed=11)
+        cpu = {"value": f / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} random causal rows of {wp.name} (explicit Sigma_KV, fp64), "
+                         f"{secs:.1f} s"}
+
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms_max / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wp.name, "decode_workload": wd.name,
+                   "step": "prefill 0.6B-shaped + decode B64 ctx8192",
+                   "l2": "inputs larger than L2 (prefill 256 MB, decode 2.1 GB); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel",
+                     "achieved": wp.flops / pre_launch_s / 1e12, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": wp.flops / pre_launch_s / 1e12 / tc_peak,
+                     "peak_source": f"bf16_tflops ({'of measured' if peaks_src == 'measured' else 'of fallback'})",
+                     "traffic": NCU_TRAFFIC_BYTES["prefill_tc_kernel"],
+                     "algorithmic_flops_per_launch": wp.flops},
+        "decode": {"workload": wd.name, "value": dec_gbs, "unit": "GB/s",
+                   "ms": dec_launch_s * 1e3,
+                   "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + combine",
+                                "achieved": dbytes / dec_launch_s / 1e9, "peak": hbm_peak,
+                                "unit": "GB/s", "frac": dbytes / dec_launch_s / 1e9 / hbm_peak,
+                                "peak_source": f"hbm_gbs ({peaks_src})",
+                                "traffic": NCU_TRAFFIC_BYTES["decode_split_kernel"],
+                                "algorithmic_bytes_per_launch": dbytes}},
+        "extra": extra,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "gpu": torch.cuda.get_device_name(dev),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,141 @@
+/*
+ * plx.h -- C ABI of libplx.so, the GB300 (sm_103a) Parallax attention forward.
+ *
+ * Parallax ("Parallax: parametrized local linear attention for language
+ * modeling", section "Core mechanism", output equation) corrects causal
+ * softmax attention by the softmax-weighted KV cross-covariance seen by each
+ * query, probed by a learned per-query vector rho_i = W_R x_i:
+ *
+ *     o_i = o^SA_i - Sigma_KV^(i) rho_i
+ *     w_ij = softmax_j(q_i . k_j / sqrt(d)),   o^SA_i = sum_j w_ij v_j
+ *     Sigma_KV^(i) = sum_j w_ij (v_j - o^SA_i)(k_j - mu_i)^T,  mu_i = sum_j w_ij k_j
+ *
+ * The kernels never form Sigma. They stream the keys once, as the pages'
+ * FlashAttention-compatible streaming algorithm (section "Hardware-aware
+ * algorithm") does, using the exact identity
+ *
+ *     o = O1 - O2 + O1 * s,  T_ij = rho_i . k_j,  O1 = P V,  O2 = (P o T) V,
+ *     s = rowsum(P o T)      (P the softmax weights)
+ *
+ * which follows because sum_j w_ij (v_j - o^SA_i) = 0 removes the mu term.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no reference after the call returns. Every call is asynchronous
+ *     and ordered on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Tensors are dense and contiguous, head dimension d innermost.
+ *   - Query head h reads KV head h / (Hq / Hkv) (consecutive grouping, GQA).
+ *   - Softmax scale is 1/sqrt(d); causal masking keeps keys j <= i; T uses
+ *     the raw keys (any scale of the probe lives in W_R).
+ *   - Inputs must be finite. A gate on the correction branch is applied by
+ *     the caller by scaling r (the correction is linear in rho).
+ *   - Arguments are validated on the host before any launch; a rejected call
+ *     launches nothing and returns PLX_ERR_INVALID_ARG or PLX_ERR_UNSUPPORTED.
+ *     plx_last_error_message() then says which argument was wrong.
+ *   - Every wait inside a kernel is bounded. A wait that runs out sets a
+ *     device error word instead of hanging; plx_check_device_error() reads
+ *     (and clears) it and returns PLX_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef PLX_H
+#define PLX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int plx_status;
+
+#define PLX_OK 0
+#define PLX_ERR_INVALID_ARG 1    /* null / misaligned pointer, bad size or ratio */
+#define PLX_ERR_UNSUPPORTED 2    /* valid but not implemented (e.g. head dim) */
+#define PLX_ERR_CUDA 3           /* a CUDA runtime or driver call failed */
+#define PLX_ERR_DEVICE_TIMEOUT 4 /* a bounded in-kernel wait ran out */
+
+/*
+ * Causal prefill, bf16 in / bf16 out, fp32 accumulation (tcgen05 tensor cores).
+ *   q, r  : bf16 [B, Hq, L, d]   queries and probes rho (one probe per query head)
+ *   k, v  : bf16 [B, Hkv, L, d]
+ *   out   : bf16 [B, Hq, L, d]   o = o^SA - Sigma_KV rho, rounded to nearest even
+ *   lse   : fp32 [B, Hq, L]      natural-log log-sum-exp of the scaled scores;
+ *                                may be NULL
+ *   d must be 128; Hq % Hkv == 0; B, Hq, Hkv, L >= 1; every pointer 16-byte
+ *   aligned (TMA). Requires an sm_100-family GPU with tcgen05 (sm_103a build).
+ */
+plx_status plx_prefill_fwd(const void *q, const void *k, const void *v, const void *r,
+                           void *out, float *lse, int B, int Hq, int Hkv, int L, int d,
+                           void *stream);
+
+/*
+ * Causal prefill in fp32 (CUDA cores, fp32 arithmetic throughout). Same
+ * arguments and layouts as plx_prefill_fwd with float tensors; d in {64, 128}.
+ * This is the exact-arithmetic path used to check parity at 1e-5 relative error.
+ */
+plx_status plx_prefill_fwd_f32(const float *q, const float *k, const float *v, const float *r,
+                               float *out, float *lse, int B, int Hq, int Hkv, int L, int d,
+                               void *stream);
+
+/*
+ * Decode: one new query per sequence against its KV cache (split-KV + a
+ * log-sum-exp combine), bf16 in / out, fp32 accumulation.
+ *   q, r           : bf16 [B, Hq, d]
+ *   kcache, vcache : bf16 packed [sum_b seqlens[b], Hkv, d]; sequence b starts
+ *                    at token sum_{b' < b} seqlens[b']. The cache already holds
+ *                    the current token: the query sees all seqlens[b] keys.
+ *   seqlens        : int32 [B] on the device, each >= 0. A sequence of length
+ *                    0 gets an all-zero output row.
+ *   out            : bf16 [B, Hq, d]
+ *   d must be 128; Hq % Hkv == 0 and Hq / Hkv <= 8. Per-split partial results
+ *   go to a stream-ordered scratch buffer (cudaMallocAsync / cudaFreeAsync on
+ *   `stream`) sized from B, Hq, d and the split count.
+ */
+plx_status plx_decode_fwd(const void *q, const void *r, const void *kcache, const void *vcache,
+                          const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
+                          void *stream);
+
+/*
+ * plx_decode_fwd with an explicit split count (nsplit >= 1 splits per
+ * sequence, keys of split s: [ceil(len*s/nsplit), ceil(len*(s+1)/nsplit)))
+ * and a caller-provided device workspace of at least
+ * plx_decode_workspace_bytes(B, Hq, d, nsplit) bytes, 16-byte aligned.
+ * nsplit <= 0 picks the default; workspace == NULL allocates as
+ * plx_decode_fwd does. The result does not depend on nsplit beyond fp32
+ * rounding.
+ */
+plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, const void *vcache,
+                             const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
+                             int nsplit, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of decode workspace for a given split count (fp32 partials:
+ * B * Hq * nsplit * (2 d + 2) * 4). */
+size_t plx_decode_workspace_bytes(int B, int Hq, int d, int nsplit);
+
+/* The split count plx_decode_fwd uses on the current device for B sequences
+ * of Hkv KV heads (targets a few CTAs per SM; lengths are not known on the
+ * host). */
+int plx_decode_default_nsplit(int B, int Hkv);
+
+/* Synchronises `stream`, then reads and clears the device error word.
+ * PLX_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the last check,
+ * PLX_ERR_CUDA if the stream reports an error, else PLX_OK. */
+plx_status plx_check_device_error(void *stream);
+
+/* Launches one block whose wait on an mbarrier that nothing ever arrives on
+ * runs out after about `limit_cycles` SM clock cycles; the kernel then sets
+ * the device error word and returns. Exercises the failure path of the
+ * bounded waits without faulting or hanging the GPU. */
+plx_status plx_debug_timeout_probe(long long limit_cycles, void *stream);
+
+/* Static description of a status code. */
+const char *plx_status_string(plx_status s);
+
+/* Detail of the last non-OK status returned on the calling host thread. */
+const char *plx_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PLX_H */

@@ -1,0 +1,196 @@
+"""Thin ctypes binding over libplx.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (declared in
+include/plx.h) and does nothing but check tensor shapes/dtypes/devices, pass
+``data_ptr()`` values and the current CUDA stream, and turn a non-OK status
+into an exception. All arithmetic runs in the library's kernels; there is no
+fallback: if libplx.so is missing or fails to load, every call raises.
+PyTorch supplies device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libplx.so")
+
+PLX_OK = 0
+PLX_ERR_INVALID_ARG = 1
+PLX_ERR_UNSUPPORTED = 2
+PLX_ERR_CUDA = 3
+PLX_ERR_DEVICE_TIMEOUT = 4
+
+# Every symbol the header declares, with its ctypes signature.
+_vp, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
+SIGNATURES = {
+    "plx_prefill_fwd": (_i, [_vp] * 6 + [_i] * 5 + [_vp]),
+    "plx_prefill_fwd_f32": (_i, [_vp] * 6 + [_i] * 5 + [_vp]),
+    "plx_decode_fwd": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
+    "plx_decode_fwd_ex": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
+    "plx_decode_workspace_bytes": (_sz, [_i] * 4),
+    "plx_decode_default_nsplit": (_i, [_i] * 2),
+    "plx_check_device_error": (_i, [_vp]),
+    "plx_debug_timeout_probe": (_i, [_ll, _vp]),
+    "plx_status_string": (ctypes.c_char_p, [_i]),
+    "plx_last_error_message": (ctypes.c_char_p, []),
+}
+
+
+class PlxError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """Load libplx.so (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libplx.so not built ({LIB_PATH}); run "
+                    "python -m parametrized_local_linear_gb300.build")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != PLX_OK:
+        msg = lib().plx_last_error_message().decode(errors="replace")
+        raise PlxError(status, msg or lib().plx_status_string(status).decode())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, ndim, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _prefill(fn, dtype, q, k, v, r, out, lse, stream):
+    _need(q, "q", dtype, 4)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("r", r)):
+        _need(t, name, dtype, 4, dev)
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(r.shape) != tuple(q.shape):
+        raise ValueError("r must have the shape of q")
+    if tuple(k.shape) != (B, Hkv, L, d) or tuple(v.shape) != (B, Hkv, L, d):
+        raise ValueError("k and v must be [B, Hkv, L, d] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dtype, 4, dev)
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have the shape of q")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3, dev)
+        if tuple(lse.shape) != (B, Hq, L):
+            raise ValueError("lse must be [B, Hq, L]")
+    with torch.cuda.device(dev):
+        st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(), out.data_ptr(),
+                lse.data_ptr() if lse is not None else None, B, Hq, Hkv, L, d,
+                _stream(stream, dev))
+    _check(st)
+    return out, lse
+
+
+def plx_prefill_fwd(q, k, v, r, out=None, lse=None, stream=None):
+    """Causal Parallax prefill, bf16 (see include/plx.h). Returns (out, lse)."""
+    return _prefill(lib().plx_prefill_fwd, torch.bfloat16, q, k, v, r, out, lse, stream)
+
+
+def plx_prefill_fwd_f32(q, k, v, r, out=None, lse=None, stream=None):
+    """Causal Parallax prefill, fp32 (see include/plx.h). Returns (out, lse)."""
+    return _prefill(lib().plx_prefill_fwd_f32, torch.float32, q, k, v, r, out, lse, stream)
+
+
+def plx_decode_fwd(q, r, kcache, vcache, seqlens, out=None, nsplit=0, workspace=None,
+                   stream=None):
+    """Parallax decode over a packed ragged KV cache (see include/plx.h).
+
+    q, r: bf16 [B, Hq, d]; kcache, vcache: bf16 [sum(seqlens), Hkv, d];
+    seqlens: int32 [B] on the device. ``nsplit``/``workspace`` select
+    plx_decode_fwd_ex; the defaults call plx_decode_fwd. Returns out.
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    _need(r, "r", torch.bfloat16, 3, dev)
+    _need(kcache, "kcache", torch.bfloat16, 3, dev)
+    _need(vcache, "vcache", torch.bfloat16, 3, dev)
+    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    B, Hq, d = q.shape
+    Hkv = kcache.shape[1]
+    if tuple(r.shape) != tuple(q.shape) or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("r must match q and vcache must match kcache")
+    if kcache.shape[2] != d or seqlens.shape[0] != B:
+        raise ValueError("kcache must be [T, Hkv, d] and seqlens [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    L = lib()
+    with torch.cuda.device(dev):
+        s = _stream(stream, dev)
+        if nsplit == 0 and workspace is None:
+            st = L.plx_decode_fwd(q.data_ptr(), r.data_ptr(), kcache.data_ptr(), vcache.data_ptr(),
+                                  seqlens.data_ptr(), out.data_ptr(), B, Hq, Hkv, d, s)
+        else:
+            ws_ptr, ws_bytes = None, 0
+            if workspace is not None:
+                if not workspace.is_cuda or workspace.device != dev:
+                    raise ValueError("workspace must be on the device of q")
+                ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+            st = L.plx_decode_fwd_ex(q.data_ptr(), r.data_ptr(), kcache.data_ptr(),
+                                     vcache.data_ptr(), seqlens.data_ptr(), out.data_ptr(), B, Hq,
+                                     Hkv, d, int(nsplit), ws_ptr, ws_bytes, s)
+    _check(st)
+    return out
+
+
+def plx_decode_workspace_bytes(B, Hq, d, nsplit) -> int:
+    return int(lib().plx_decode_workspace_bytes(B, Hq, d, nsplit))
+
+
+def plx_decode_default_nsplit(B, Hkv) -> int:
+    return int(lib().plx_decode_default_nsplit(B, Hkv))
+
+
+def plx_check_device_error(stream=None, device=None):
+    """Synchronise the stream and raise PlxError if a bounded wait ran out."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(lib().plx_check_device_error(_stream(stream, dev)))
+
+
+def plx_debug_timeout_probe(limit_cycles=100000, stream=None):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _check(lib().plx_debug_timeout_probe(int(limit_cycles), _stream(stream, dev)))

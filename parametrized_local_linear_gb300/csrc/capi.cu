@@ -1,0 +1,268 @@
+// C ABI of libplx.so: argument validation, per-device set-up, the decode
+// workspace, device error reporting. The operations themselves are defined
+// in include/plx.h; the kernels live in prefill_tc.cu, prefill_f32.cu and
+// decode.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "../../include/plx.h"
+#include "plx_device.cuh"
+#include "plx_internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+plx_status fail(plx_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+plx_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(PLX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device error word: one per device (a __device__ variable is instantiated per
+// device), its address resolved once per device.
+__device__ unsigned g_plx_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+int current_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+
+// Probe kernel for the bounded-wait failure path: wait on an mbarrier that
+// nothing will ever arrive on.
+__global__ void timeout_probe_kernel(long long limit, unsigned *err) {
+  __shared__ uint64_t bar;
+  __shared__ int flag;
+  if (threadIdx.x == 0) {
+    plx::mbar_init(plx::smem_u32(&bar), 1);
+    flag = 0;
+    plx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const plx::Abort ab{&flag, err};
+    plx::mbar_wait(plx::smem_u32(&bar), 0, ab, limit);
+  }
+}
+
+}  // namespace
+
+namespace plx {
+
+unsigned *device_error_word() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_plx_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned *>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+cudaError_t launch_timeout_probe(long long limit_cycles, unsigned *err, cudaStream_t stream) {
+  timeout_probe_kernel<<<1, 32, 0, stream>>>(limit_cycles, err);
+  return cudaGetLastError();
+}
+
+}  // namespace plx
+
+namespace {
+
+plx_status check_common(const char *fn, int B, int Hq, int Hkv, int L, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || L < 1 || d < 1)
+    return fail(PLX_ERR_INVALID_ARG, "%s: sizes must be >= 1 (B=%d Hq=%d Hkv=%d L=%d d=%d)", fn, B,
+                Hq, Hkv, L, d);
+  if (Hq % Hkv != 0)
+    return fail(PLX_ERR_INVALID_ARG, "%s: Hq (%d) must be a multiple of Hkv (%d)", fn, Hq, Hkv);
+  return PLX_OK;
+}
+
+plx_status finish_launch(cudaError_t e, const char *fn) {
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return PLX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+plx_status plx_prefill_fwd(const void *q, const void *k, const void *v, const void *r, void *out,
+                           float *lse, int B, int Hq, int Hkv, int L, int d, void *stream) {
+  const char *fn = "plx_prefill_fwd";
+  if (!q || !k || !v || !r || !out) return fail(PLX_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
+  plx_status s = check_common(fn, B, Hq, Hkv, L, d);
+  if (s) return s;
+  if (d != 128) return fail(PLX_ERR_UNSUPPORTED, "%s: head dim %d (only 128)", fn, d);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(r) || !aligned16(out))
+    return fail(PLX_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", fn);
+  if (static_cast<long long>(L + 127) / 128 * Hq * B > 0x7fffffffLL || static_cast<long long>(B) * Hq > 0x7fffffff)
+    return fail(PLX_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
+  return finish_launch(plx::launch_prefill_tc(q, k, v, r, out, lse, B, Hq, Hkv, L,
+                                              plx::device_error_word(),
+                                              static_cast<cudaStream_t>(stream)),
+                       fn);
+}
+
+plx_status plx_prefill_fwd_f32(const float *q, const float *k, const float *v, const float *r,
+                               float *out, float *lse, int B, int Hq, int Hkv, int L, int d,
+                               void *stream) {
+  const char *fn = "plx_prefill_fwd_f32";
+  if (!q || !k || !v || !r || !out) return fail(PLX_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
+  plx_status s = check_common(fn, B, Hq, Hkv, L, d);
+  if (s) return s;
+  if (d != 64 && d != 128) return fail(PLX_ERR_UNSUPPORTED, "%s: head dim %d (64 or 128)", fn, d);
+  if (B > 65535 || Hq > 65535)
+    return fail(PLX_ERR_UNSUPPORTED, "%s: B and Hq must be <= 65535", fn);
+  return finish_launch(plx::launch_prefill_f32(q, k, v, r, out, lse, B, Hq, Hkv, L, d,
+                                               plx::device_error_word(),
+                                               static_cast<cudaStream_t>(stream)),
+                       fn);
+}
+
+size_t plx_decode_workspace_bytes(int B, int Hq, int d, int nsplit) {
+  if (B < 1 || Hq < 1 || d < 1 || nsplit < 1) return 0;
+  return static_cast<size_t>(B) * Hq * nsplit * (2 * static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+int plx_decode_default_nsplit(int B, int Hkv) {
+  if (B < 1 || Hkv < 1) return 1;
+  // Lengths live on the device, so the split count cannot look at them: aim
+  // for about 32 CTAs per SM in total, which keeps the largest split of a
+  // ragged batch small against the whole job.
+  const long long target = 32LL * plx::sm_count();
+  long long n = (target + static_cast<long long>(B) * Hkv - 1) / (static_cast<long long>(B) * Hkv);
+  if (n < 1) n = 1;
+  if (n > 256) n = 256;
+  return static_cast<int>(n);
+}
+
+plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, const void *vcache,
+                             const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
+                             int nsplit, void *workspace, size_t workspace_bytes, void *stream) {
+  const char *fn = "plx_decode_fwd";
+  if (!q || !r || !kcache || !vcache || !seqlens || !out)
+    return fail(PLX_ERR_INVALID_ARG, "%s: null pointer", fn);
+  plx_status s = check_common(fn, B, Hq, Hkv, 1, d);
+  if (s) return s;
+  if (d != 128) return fail(PLX_ERR_UNSUPPORTED, "%s: head dim %d (only 128)", fn, d);
+  if (Hq / Hkv > 8) return fail(PLX_ERR_UNSUPPORTED, "%s: Hq / Hkv = %d (at most 8)", fn, Hq / Hkv);
+  if (B > 65535 || Hkv > 65535) return fail(PLX_ERR_UNSUPPORTED, "%s: B and Hkv must be <= 65535", fn);
+  if (!aligned16(q) || !aligned16(r) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+    return fail(PLX_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", fn);
+  if (nsplit <= 0) nsplit = plx_decode_default_nsplit(B, Hkv);
+  if (nsplit > 65535) return fail(PLX_ERR_INVALID_ARG, "%s: nsplit %d too large", fn, nsplit);
+  const size_t need = plx_decode_workspace_bytes(B, Hq, d, nsplit);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (workspace != nullptr) {
+    if (workspace_bytes < need)
+      return fail(PLX_ERR_INVALID_ARG, "%s: workspace of %zu bytes, need %zu", fn, workspace_bytes,
+                  need);
+    if (!aligned16(workspace)) return fail(PLX_ERR_INVALID_ARG, "%s: workspace not 16-byte aligned", fn);
+    return finish_launch(plx::launch_decode(q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, nsplit,
+                                            static_cast<float *>(workspace),
+                                            plx::device_error_word(), st),
+                         fn);
+  }
+  void *ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, need, st);
+  if (e != cudaSuccess) return cuda_fail(e, "plx_decode_fwd: workspace allocation");
+  e = plx::launch_decode(q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, nsplit,
+                         static_cast<float *>(ws), plx::device_error_word(), st);
+  cudaError_t e2 = cudaFreeAsync(ws, st);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  if (e2 != cudaSuccess) return cuda_fail(e2, "plx_decode_fwd: workspace release");
+  return PLX_OK;
+}
+
+plx_status plx_decode_fwd(const void *q, const void *r, const void *kcache, const void *vcache,
+                          const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
+                          void *stream) {
+  return plx_decode_fwd_ex(q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, d, 0, nullptr, 0,
+                           stream);
+}
+
+plx_status plx_check_device_error(void *stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "plx_check_device_error: stream");
+  unsigned *w = plx::device_error_word();
+  if (w == nullptr) return fail(PLX_ERR_CUDA, "plx_check_device_error: no error word");
+  unsigned v = 0;
+  e = cudaMemcpyAsync(&v, w, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w, 0, sizeof(unsigned), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "plx_check_device_error: read");
+  if (v & plx::kErrTimeout)
+    return fail(PLX_ERR_DEVICE_TIMEOUT, "a bounded in-kernel wait ran out (error word 0x%x)", v);
+  return PLX_OK;
+}
+
+plx_status plx_debug_timeout_probe(long long limit_cycles, void *stream) {
+  if (limit_cycles < 0 || limit_cycles > (1LL << 32))
+    return fail(PLX_ERR_INVALID_ARG, "plx_debug_timeout_probe: limit out of range");
+  return finish_launch(plx::launch_timeout_probe(limit_cycles, plx::device_error_word(),
+                                                 static_cast<cudaStream_t>(stream)),
+                       "plx_debug_timeout_probe");
+}
+
+const char *plx_status_string(plx_status s) {
+  switch (s) {
+    case PLX_OK: return "ok";
+    case PLX_ERR_INVALID_ARG: return "invalid argument";
+    case PLX_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PLX_ERR_CUDA: return "CUDA error";
+    case PLX_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char *plx_last_error_message(void) { return g_msg; }
+
+}  // extern "C"

@@ -1,0 +1,345 @@
+// Parallax decode: split-KV streaming over a packed bf16 KV cache, then a
+// log-sum-exp combine of the per-split partial results.
+//
+// The method ("Parallax: parametrized local linear attention for language
+// modeling", sections "Core mechanism" and "Hardware-aware algorithm") adds a
+// covariance branch to softmax attention that reads the same KV stream; the
+// pages' decode kernel therefore computes q.k and rho.k in the same tensor-core
+// instructions so the cache is read from HBM once for both branches. This
+// kernel does the same on sm_103a with warp-level mma.sync:
+//
+//   CTA (split s, kv head g, sequence b), 4 consumer warps + 1 producer warp.
+//   Producer: 1-D bulk TMA copies of the 256-byte K and V rows of its key
+//     range into a ring of shared-memory stages (row pitch 272 B, so ldmatrix
+//     is bank-conflict free), completion counted on per-stage mbarriers.
+//   Consumers: stages are dealt round-robin to the 4 warps. For each 16 keys
+//     one m16n8k16 product gives all four dot-product families at once: A rows
+//     0..G-1 hold the G query heads' q, rows 8..8+G-1 their probes r, so the
+//     accumulator row g is the score s = q.k and row g + 8 is t = r.k for the
+//     same key in the same thread. P and P*T then form the A operand of the
+//     value product (rows g: P -> O1, rows g + 8: P*T -> O2), again in
+//     registers, with V^T read by ldmatrix.trans.
+//   Each warp runs the online-softmax recurrence (running max m, denominator
+//   l, sigma = sum p t, O1 and O2 accumulators, all rescaled together); the
+//   warps are merged in shared memory and the CTA writes one partial record
+//   per query head: (O1/l, O2/l, sigma/l, log2-sum-exp) in fp32.
+//
+// The combine kernel merges the records of a (sequence, head) with weights
+// 2^(lse_s - max) and only then forms o = O1 - O2 + O1 * s. Combining final
+// per-split outputs would be wrong: O1 * s is bilinear in the partial sums.
+#include <math.h>
+
+#include "plx_device.cuh"
+#include "plx_internal.h"
+
+namespace plx {
+namespace {
+
+constexpr int D = 128;
+constexpr int KT = 32;                        // keys per stage
+constexpr int NST = 6;                        // stages in the ring
+constexpr int NCW = 4;                        // consumer warps
+constexpr int ROWB = D * 2 + 16;              // padded row pitch in shared memory
+constexpr int STAGE_BYTES = 2 * KT * ROWB;    // K rows then V rows
+constexpr int OFF_BAR = NST * STAGE_BYTES;    // 104448
+constexpr int SMEM_BYTES = OFF_BAR + 2 * NST * 8 + 16;
+constexpr int REC = 2 * D + 2;                // floats per partial record
+constexpr int THREADS = 32 * (NCW + 1);
+
+struct DecodeArgs {
+  const __nv_bfloat16 *q, *r, *kc, *vc;
+  const int *seqlens;
+  float *ws;
+  int B, Hq, Hkv, G, nsplit;
+  float scale_log2;  // log2(e) / sqrt(d)
+  unsigned *err;
+};
+
+__global__ void __launch_bounds__(THREADS) decode_split_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+  uint64_t *empty = full + NST;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NST);
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int len = a.seqlens[b];
+  const int lo = static_cast<int>((static_cast<long long>(len) * split + a.nsplit - 1) / a.nsplit);
+  const int hi =
+      static_cast<int>((static_cast<long long>(len) * (split + 1) + a.nsplit - 1) / a.nsplit);
+  const int nkeys = hi - lo;
+  const int ntiles = (nkeys + KT - 1) / KT;
+
+  // Zero the stages once so rows a partial last tile does not fill hold finite
+  // data (their weights are zero; 0 * finite stays 0 in the value product).
+  for (int i = threadIdx.x; i < OFF_BAR / 16; i += THREADS)
+    reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  const Abort ab{abort_flag, a.err};
+
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    long long off = 0;
+    for (int i = lane; i < b; i += 32) off += a.seqlens[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
+    const size_t row_pitch = static_cast<size_t>(a.Hkv) * D;  // elements between tokens
+    const __nv_bfloat16 *kbase = a.kc + (static_cast<size_t>(off + lo) * a.Hkv + kvh) * D;
+    const __nv_bfloat16 *vbase = a.vc + (static_cast<size_t>(off + lo) * a.Hkv + kvh) * D;
+    int issued = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % NST;
+      if (t >= NST) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(smem_u32(&empty[st]), ((t / NST) - 1) & 1, ab);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      const int nvalid = min(KT, nkeys - t * KT);
+      const uint32_t bar = smem_u32(&full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nvalid) * 2u * D * 2u);
+      __syncwarp();
+      if (lane < nvalid) {
+        const size_t tok = static_cast<size_t>(t) * KT + lane;
+        const uint32_t dst = smem_u32(smem + st * STAGE_BYTES + lane * ROWB);
+        bulk_g2s(dst, kbase + tok * row_pitch, D * 2, bar);
+        bulk_g2s(dst + KT * ROWB, vbase + tok * row_pitch, D * 2, bar);
+      }
+      issued = t + 1;
+    }
+    if (ab.raised() && lane == 0) {
+      // Let this warp's own copies land before the CTA exits.
+      for (int t = max(0, issued - NST); t < issued; ++t)
+        mbar_wait_drain(smem_u32(&full[t % NST]), (t / NST) & 1);
+    }
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int g = lane >> 2, tq = lane & 3;
+  float acc[16][4];
+  float m = -INFINITY, l = 0.f, sg = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  if (warp < NCW) {
+    uint32_t qa[8][4];
+    {
+      const bool live = g < a.G;
+      const size_t hrow = (static_cast<size_t>(b) * a.Hq + kvh * a.G + (live ? g : 0)) * D;
+      const uint32_t *qr = reinterpret_cast<const uint32_t *>(a.q + hrow);
+      const uint32_t *rr = reinterpret_cast<const uint32_t *>(a.r + hrow);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qa[kk][0] = live ? qr[8 * kk + tq] : 0u;
+        qa[kk][1] = live ? rr[8 * kk + tq] : 0u;
+        qa[kk][2] = live ? qr[8 * kk + 4 + tq] : 0u;
+        qa[kk][3] = live ? rr[8 * kk + 4 + tq] : 0u;
+      }
+    }
+    for (int t = warp; t < ntiles; t += NCW) {
+      const int st = t % NST;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(smem_u32(&full[st]), (t / NST) & 1, ab);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const uint32_t kb = smem_u32(smem + st * STAGE_BYTES);
+      const uint32_t vb = kb + KT * ROWB;
+#pragma unroll
+      for (int half = 0; half < KT / 16; ++half) {
+        const int key0 = t * KT + half * 16;
+        if (key0 >= nkeys) break;
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const uint32_t krow = kb + (half * 16 + (lane >> 4) * 8 + (lane & 7)) * ROWB +
+                              ((lane >> 3) & 1) * 16;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(krow + kk * 32, b0, b1, b2, b3);
+          mma_bf16_16816(c[0], qa[kk], b0, b1);
+          mma_bf16_16816(c[1], qa[kk], b2, b3);
+        }
+        // c[n][0..1]: s for keys key0 + 8n + 2tq + {0,1}; c[n][2..3]: t for the same keys.
+        float s[2][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = key0 + 8 * n + 2 * tq + e;
+            s[n][e] = key < nkeys ? c[n][e] * a.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, s[n][e]);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m, mx);
+        const float msub = mn == -INFINITY ? 0.f : mn;
+        const float alpha = fast_exp2(m - msub);  // m = -inf: 0
+        float p[2][2], pt[2][2], ps = 0.f, pts = 0.f;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            p[n][e] = fast_exp2(s[n][e] - msub);
+            pt[n][e] = p[n][e] * c[n][2 + e];
+            ps += p[n][e];
+            pts += pt[n][e];
+          }
+        l = fmaf(l, alpha, ps);
+        sg = fmaf(sg, alpha, pts);
+        m = mn;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            acc[i][0] *= alpha; acc[i][1] *= alpha; acc[i][2] *= alpha; acc[i][3] *= alpha;
+          }
+        }
+        const uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(pt[0][0], pt[0][1]),
+                                pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(pt[1][0], pt[1][1])};
+        const uint32_t vrow = vb + (half * 16 + ((lane >> 3) & 1) * 8 + (lane & 7)) * ROWB +
+                              (lane >> 4) * 16;
+#pragma unroll
+        for (int nd = 0; nd < 8; ++nd) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vrow + nd * 32, b0, b1, b2, b3);
+          mma_bf16_16816(acc[2 * nd], pa, b0, b1);
+          mma_bf16_16816(acc[2 * nd + 1], pa, b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
+    }
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    sg += __shfl_xor_sync(0xffffffffu, sg, 1);
+    sg += __shfl_xor_sync(0xffffffffu, sg, 2);
+  }
+
+  // ------------------------------------------------------------ merge warps
+  __syncthreads();  // every stage is consumed (or the CTA aborted): reuse them
+  float *red = reinterpret_cast<float *>(smem);          // [NCW][2G][D]
+  float *mls = red + NCW * 2 * a.G * D;                   // [NCW][G][3]
+  if (warp < NCW && g < a.G) {
+    float *o1 = red + (warp * 2 * a.G + g) * D;
+    float *o2 = red + (warp * 2 * a.G + a.G + g) * D;
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+      o1[8 * nd + 2 * tq] = acc[nd][0];
+      o1[8 * nd + 2 * tq + 1] = acc[nd][1];
+      o2[8 * nd + 2 * tq] = acc[nd][2];
+      o2[8 * nd + 2 * tq + 1] = acc[nd][3];
+    }
+    if (tq == 0) {
+      mls[(warp * a.G + g) * 3 + 0] = m;
+      mls[(warp * a.G + g) * 3 + 1] = l;
+      mls[(warp * a.G + g) * 3 + 2] = sg;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < D) {
+    const int dim = threadIdx.x;
+    for (int gh = 0; gh < a.G; ++gh) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, mls[(w * a.G + gh) * 3]);
+      float *rec = a.ws + ((static_cast<size_t>(b) * a.Hq + kvh * a.G + gh) * a.nsplit + split) * REC;
+      if (M == -INFINITY || ab.raised()) {
+        rec[dim] = 0.f;
+        rec[D + dim] = 0.f;
+        if (dim == 0) {
+          rec[2 * D] = 0.f;
+          rec[2 * D + 1] = -INFINITY;
+        }
+        continue;
+      }
+      float L = 0.f, S = 0.f, O1 = 0.f, O2 = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) {
+        const float f = fast_exp2(mls[(w * a.G + gh) * 3] - M);
+        L = fmaf(f, mls[(w * a.G + gh) * 3 + 1], L);
+        S = fmaf(f, mls[(w * a.G + gh) * 3 + 2], S);
+        O1 = fmaf(f, red[(w * 2 * a.G + gh) * D + dim], O1);
+        O2 = fmaf(f, red[(w * 2 * a.G + a.G + gh) * D + dim], O2);
+      }
+      const float inv = 1.f / L;
+      rec[dim] = O1 * inv;
+      rec[D + dim] = O2 * inv;
+      if (dim == 0) {
+        rec[2 * D] = S * inv;
+        rec[2 * D + 1] = M + log2f(L);
+      }
+    }
+  }
+}
+
+// One block of D threads per (sequence, query head): merge the splits.
+__global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ ws,
+                                                          __nv_bfloat16 *__restrict__ out,
+                                                          int nsplit) {
+  const int bh = blockIdx.x, dim = threadIdx.x;
+  const float *rec = ws + static_cast<size_t>(bh) * nsplit * REC;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, rec[s * REC + 2 * D + 1]);
+  float o = 0.f;
+  if (M != -INFINITY) {
+    float W = 0.f, o1 = 0.f, o2 = 0.f, sf = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float lse = rec[s * REC + 2 * D + 1];
+      const float w = exp2f(lse - M);  // empty split: lse = -inf, w = 0
+      W += w;
+      o1 = fmaf(w, rec[s * REC + dim], o1);
+      o2 = fmaf(w, rec[s * REC + D + dim], o2);
+      sf = fmaf(w, rec[s * REC + 2 * D], sf);
+    }
+    const float inv = 1.f / W;
+    o1 *= inv;
+    o2 *= inv;
+    sf *= inv;
+    o = o1 - o2 + o1 * sf;
+  }
+  out[static_cast<size_t>(bh) * D + dim] = __float2bfloat16_rn(o);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void *q, const void *r, const void *kcache, const void *vcache,
+                          const int *seqlens, void *out, int B, int Hq, int Hkv, int nsplit,
+                          float *workspace, unsigned *err, cudaStream_t stream) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  DecodeArgs a;
+  a.q = static_cast<const __nv_bfloat16 *>(q);
+  a.r = static_cast<const __nv_bfloat16 *>(r);
+  a.kc = static_cast<const __nv_bfloat16 *>(kcache);
+  a.vc = static_cast<const __nv_bfloat16 *>(vcache);
+  a.seqlens = seqlens;
+  a.ws = workspace;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.nsplit = nsplit;
+  a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+  a.err = err;
+  decode_split_kernel<<<dim3(nsplit, Hkv, B), THREADS, SMEM_BYTES, stream>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_combine_kernel<<<B * Hq, D, 0, stream>>>(workspace, static_cast<__nv_bfloat16 *>(out),
+                                                  nsplit);
+  return cudaGetLastError();
+}
+
+}  // namespace plx

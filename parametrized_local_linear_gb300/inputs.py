@@ -21,12 +21,12 @@ _CHUNK = 1 << 26  # elements drawn per randn call
 
 
 def _randn(shape, gen, dtype, std=1.0):
-    out = torch.empty(shape, dtype=dtype)
+    out = torch.empty(shape, dtype=dtype, device=gen.device)
     flat = out.view(-1)
     n = flat.numel()
     for s in range(0, n, _CHUNK):
         e = min(n, s + _CHUNK)
-        x = torch.randn(e - s, generator=gen, dtype=torch.float32)
+        x = torch.randn(e - s, generator=gen, dtype=torch.float32, device=gen.device)
         if std != 1.0:
             x.mul_(std)
         flat[s:e] = x.to(dtype)
@@ -101,9 +101,11 @@ WORKLOADS = {w.name: w for w in (TINY_PREFILL_F32, PREFILL_0P6B, PREFILL_1P7B, D
                                  DECODE_RAGGED)}
 
 
-def prefill_inputs(B, Hq, Hkv, L, d, dtype=torch.bfloat16, r_std=0.05, seed=0):
-    """q, k, v, r on the CPU: q, r [B, Hq, L, d]; k, v [B, Hkv, L, d]."""
-    gen = torch.Generator().manual_seed(seed)
+def prefill_inputs(B, Hq, Hkv, L, d, dtype=torch.bfloat16, r_std=0.05, seed=0, device="cpu"):
+    """q, k, v, r: q, r [B, Hq, L, d]; k, v [B, Hkv, L, d]. Drawn on the CPU
+    unless ``device`` is a CUDA device (then drawn there: same distribution,
+    different values; used only where nothing compares against a CPU draw)."""
+    gen = torch.Generator(device=device).manual_seed(seed)
     q = _randn((B, Hq, L, d), gen, dtype)
     k = _randn((B, Hkv, L, d), gen, dtype)
     v = _randn((B, Hkv, L, d), gen, dtype)
@@ -111,14 +113,15 @@ def prefill_inputs(B, Hq, Hkv, L, d, dtype=torch.bfloat16, r_std=0.05, seed=0):
     return q, k, v, r
 
 
-def prefill_inputs_for(w: PrefillShape):
-    return prefill_inputs(w.B, w.Hq, w.Hkv, w.L, w.d, w.dtype, w.r_std, w.seed)
+def prefill_inputs_for(w: PrefillShape, device="cpu"):
+    return prefill_inputs(w.B, w.Hq, w.Hkv, w.L, w.d, w.dtype, w.r_std, w.seed, device)
 
 
-def decode_inputs(B, Hq, Hkv, d, seqlens, dtype=torch.bfloat16, r_std=0.05, seed=0):
-    """q, r [B, Hq, d]; kcache, vcache packed [sum(seqlens), Hkv, d]."""
+def decode_inputs(B, Hq, Hkv, d, seqlens, dtype=torch.bfloat16, r_std=0.05, seed=0, device="cpu"):
+    """q, r [B, Hq, d]; kcache, vcache packed [sum(seqlens), Hkv, d]; seqlens
+    int32 [B] (on the CPU). Drawn on ``device`` as in prefill_inputs."""
     seqlens = torch.as_tensor(seqlens, dtype=torch.int32)
-    gen = torch.Generator().manual_seed(seed + 7919)
+    gen = torch.Generator(device=device).manual_seed(seed + 7919)
     T = int(seqlens.sum())
     q = _randn((B, Hq, d), gen, dtype)
     r = _randn((B, Hq, d), gen, dtype, r_std)
@@ -127,5 +130,5 @@ def decode_inputs(B, Hq, Hkv, d, seqlens, dtype=torch.bfloat16, r_std=0.05, seed
     return q, r, kc, vc, seqlens
 
 
-def decode_inputs_for(w: DecodeShape):
-    return decode_inputs(w.B, w.Hq, w.Hkv, w.d, w.seqlens(), w.dtype, w.r_std, w.seed)
+def decode_inputs_for(w: DecodeShape, device="cpu"):
+    return decode_inputs(w.B, w.Hq, w.Hkv, w.d, w.seqlens(), w.dtype, w.r_std, w.seed, device)

@@ -1,0 +1,60 @@
+"""Shared helpers for the parity tests (tolerances, row sampling, device setup)."""
+import math
+import random
+
+import numpy as np
+import torch
+
+# bf16 inputs, fp32 accumulation: max|err| <= 1e-2 * max|o_ref| + 2e-3.
+BF16_REL, BF16_ABS = 1e-2, 2e-3
+# fp32 path: max|err| / max|o_ref| <= 1e-5 (and the same for lse on |lse|).
+F32_REL = 1e-5
+
+
+def device():
+    from parametrized_local_linear_gb300 import build
+    build.build()
+    return torch.device("cuda", 0)
+
+
+def assert_bf16_close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.max(np.abs(got - ref)) if got.size else 0.0
+    bound = BF16_REL * np.max(np.abs(ref)) + BF16_ABS if ref.size else 0.0
+    assert err <= bound, f"{what}: max|err| {err:.3e} > {bound:.3e}"
+    return err, bound
+
+
+def assert_f32_close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    rel = np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30)
+    assert rel <= F32_REL, f"{what}: relative error {rel:.3e} > {F32_REL:.0e}"
+    return rel
+
+
+def sample_rows(B, Hq, L, n_random, seed):
+    """The fixed edge rows of every tile boundary that matters plus a seeded
+    random set, spread over (batch, head)."""
+    rng = random.Random(seed)
+    fixed = sorted({i for i in (0, 1, 63, 64, 127, 128, 129, L // 2, L - 2, L - 1) if 0 <= i < L})
+    rows = set()
+    for n, i in enumerate(fixed):
+        rows.add((n % B, (3 * n) % Hq, i))
+    rows.add((B - 1, Hq - 1, L - 1))
+    while len(rows) < len(fixed) + 1 + n_random:
+        rows.add((rng.randrange(B), rng.randrange(Hq), rng.randrange(L)))
+    return sorted(rows)
+
+
+def tolerance_note():
+    return f"bf16: {BF16_REL}*max|ref| + {BF16_ABS}; fp32: {F32_REL} relative"
+
+
+def tau(d):
+    return 1.0 / math.sqrt(d)

@@ -1,0 +1,87 @@
+"""The C-ABI library loads and exports every entry point include/plx.h
+declares, and its host-side argument checks reject bad calls before any CUDA
+call is made (CPU only: nothing here launches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from parametrized_local_linear_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "plx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(plx_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("plx_prefill_fwd", "plx_prefill_fwd_f32", "plx_decode_fwd", "plx_status_string"):
+        assert s in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+        assert s in binding.SIGNATURES, f"binding lacks a signature for {s}"
+
+
+def test_status_strings(lib):
+    assert lib.plx_status_string(0) == b"ok"
+    assert b"timed out" in lib.plx_status_string(4)
+    assert lib.plx_status_string(99) == b"unknown status"
+
+
+def _call_prefill(lib, fn, ptr, B=1, Hq=2, Hkv=1, L=16, d=128):
+    p = ctypes.c_void_p(ptr)
+    return getattr(lib, fn)(p, p, p, p, p, None, B, Hq, Hkv, L, d, None)
+
+
+@pytest.mark.parametrize("fn", ["plx_prefill_fwd", "plx_prefill_fwd_f32"])
+def test_prefill_rejects_bad_arguments(lib, fn):
+    assert _call_prefill(lib, fn, 0) == binding.PLX_ERR_INVALID_ARG
+    assert b"null" in lib.plx_last_error_message()
+    assert _call_prefill(lib, fn, 4096, Hq=3, Hkv=2) == binding.PLX_ERR_INVALID_ARG
+    assert b"multiple" in lib.plx_last_error_message()
+    assert _call_prefill(lib, fn, 4096, L=0) == binding.PLX_ERR_INVALID_ARG
+    assert _call_prefill(lib, fn, 4096, d=96) == binding.PLX_ERR_UNSUPPORTED
+
+
+def test_prefill_bf16_rejects_misaligned(lib):
+    assert _call_prefill(lib, "plx_prefill_fwd", 4098) == binding.PLX_ERR_INVALID_ARG
+    assert b"aligned" in lib.plx_last_error_message()
+
+
+def test_decode_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(4096)
+    f = lib.plx_decode_fwd
+    assert f(None, p, p, p, p, p, 2, 4, 2, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert f(p, p, p, p, p, p, 2, 4, 2, 64, None) == binding.PLX_ERR_UNSUPPORTED
+    assert f(p, p, p, p, p, p, 2, 32, 2, 128, None) == binding.PLX_ERR_UNSUPPORTED  # G = 16
+    assert f(p, p, p, p, p, p, 2, 4, 3, 128, None) == binding.PLX_ERR_INVALID_ARG
+    ex = lib.plx_decode_fwd_ex
+    small = lib.plx_decode_workspace_bytes(2, 4, 128, 3) - 4
+    assert ex(p, p, p, p, p, p, 2, 4, 2, 128, 3, p, small, None) == binding.PLX_ERR_INVALID_ARG
+    assert b"workspace" in lib.plx_last_error_message()
+
+
+def test_workspace_size_formula(lib):
+    assert lib.plx_decode_workspace_bytes(4, 16, 128, 5) == 4 * 16 * 5 * (2 * 128 + 2) * 4
+    assert lib.plx_decode_workspace_bytes(0, 16, 128, 5) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", "/nonexistent/libplx.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.lib()

@@ -1,0 +1,99 @@
+"""GPU decode (split-KV + log-sum-exp combine) parity against the fp64 oracle."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parametrized_local_linear_gb300 import (inputs, plx_check_device_error,
+                                             plx_decode_default_nsplit, plx_decode_fwd,
+                                             plx_decode_workspace_bytes, plx_prefill_fwd)
+
+from helpers import assert_bf16_close, device
+
+pytestmark = pytest.mark.gpu
+
+
+def _to(dev, *ts):
+    return [t.to(dev) for t in ts]
+
+
+def _decode(q, r, kc, vc, sl, **kw):
+    dev = device()
+    qd, rd, kd, vd, sd = _to(dev, q, r, kc, vc, sl)
+    out = torch.full_like(qd, float("nan"))
+    plx_decode_fwd(qd, rd, kd, vd, sd, out, **kw)
+    plx_check_device_error()
+    return out.cpu()
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv", [
+    ([1, 5, 33, 0, 200, 64], 4, 2),      # includes an empty sequence and sub-tile lengths
+    ([1000, 17, 4096], 16, 8),           # model head layout
+    ([300, 301], 8, 1),                  # GQA group of 8
+])
+def test_decode_matches_oracle_all_pairs(lens, Hq, Hkv):
+    q, r, kc, vc, sl = inputs.decode_inputs(len(lens), Hq, Hkv, 128, lens, torch.bfloat16, 0.05,
+                                            len(lens) + Hq)
+    out = _decode(q, r, kc, vc, sl)
+    ref, _ = oracle.decode(q, r, kc, vc, sl)
+    assert_bf16_close(out.double().numpy(), ref, "decode")
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.all(out[b] == 0)
+
+
+@pytest.mark.parametrize("nsplit", [1, 3, 7, 64])
+def test_decode_split_count_does_not_change_the_result(nsplit):
+    lens = [700, 1, 129, 2048]
+    q, r, kc, vc, sl = inputs.decode_inputs(len(lens), 16, 8, 128, lens, torch.bfloat16, 0.05, 77)
+    base = _decode(q, r, kc, vc, sl, nsplit=1).float()
+    out = _decode(q, r, kc, vc, sl, nsplit=nsplit).float()
+    # Only fp32 summation order differs; the bf16 outputs agree to an ulp or so.
+    assert torch.max(torch.abs(out - base)) <= 2e-2 * torch.max(torch.abs(base)) + 1e-3
+
+
+def test_decode_with_caller_workspace():
+    dev = device()
+    lens = [90, 4000]
+    q, r, kc, vc, sl = inputs.decode_inputs(2, 4, 2, 128, lens, torch.bfloat16, 0.05, 8)
+    nsplit = 5
+    nbytes = plx_decode_workspace_bytes(2, 4, 128, nsplit)
+    ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=dev)
+    out = _decode(q, r, kc, vc, sl, nsplit=nsplit, workspace=ws)
+    ref, _ = oracle.decode(q, r, kc, vc, sl)
+    assert_bf16_close(out.double().numpy(), ref, "decode+workspace")
+
+
+def test_decode_equals_last_prefill_row_on_gpu():
+    """Decode over a cache equals the last row of a prefill over the same keys."""
+    dev = device()
+    L, Hq, Hkv = 333, 4, 2
+    q, k, v, r = inputs.prefill_inputs(1, Hq, Hkv, L, 128, torch.bfloat16, 0.05, 12)
+    pre, _ = plx_prefill_fwd(*_to(dev, q, k, v, r))
+    kc = k[0].permute(1, 0, 2).contiguous()  # [L, Hkv, d]
+    vc = v[0].permute(1, 0, 2).contiguous()
+    out = _decode(q[:, :, -1].contiguous(), r[:, :, -1].contiguous(), kc, vc,
+                  torch.tensor([L], dtype=torch.int32))
+    assert_bf16_close(out[0].double().numpy(), pre[0, :, -1].double().cpu().numpy(), "decode-vs-prefill")
+
+
+@pytest.mark.parametrize("w", [inputs.DECODE_B64, inputs.DECODE_RAGGED], ids=lambda w: w.name)
+def test_decode_full_size_workload_sampled_pairs(w):
+    q, r, kc, vc, sl = inputs.decode_inputs_for(w)
+    out = _decode(q, r, kc, vc, sl)
+    rng = random.Random(w.seed)
+    pairs = sorted({(0, 0), (w.B - 1, w.Hq - 1)} |
+                   {(rng.randrange(w.B), rng.randrange(w.Hq)) for _ in range(10)})
+    ref, _ = oracle.decode(q, r, kc, vc, sl, pairs=pairs, threads=8)
+    got = np.stack([out[b, h].double().numpy() for b, h in pairs])
+    assert_bf16_close(got, ref, w.name)
+    assert torch.isfinite(out).all()
+
+
+def test_default_split_count_is_sane():
+    device()
+    n = plx_decode_default_nsplit(64, 8)
+    assert 1 <= n <= 256
+    assert plx_decode_default_nsplit(1, 1) >= n
