@@ -139,6 +139,12 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def whole_job_rate(world, units_per_rank_per_step, steps, max_ms):
+    """Whole-job throughput: every rank processed the same units; the job took
+    the slowest rank's time (max over ranks)."""
+    return world * units_per_rank_per_step * steps / (max_ms * 1e-3)
+
+
 def oracle_prefill_sample(w, q, k, v, r, budget_s, seed, threads=None):
     """Time the fp64 oracle on seeded random causal rows of workload w until
     about budget_s seconds of oracle time; return (algorithmic flops of the
@@ -196,6 +202,34 @@ def run_reference(args, world, rank):
     return 0
 
 
+def run_ncu_case(case):
+    """Profiling-sized cases for ncu (one kernel, few launches, inputs > L2)."""
+    from parametrized_local_linear_gb300 import (build, plx_check_device_error, plx_decode_fwd,
+                                                 plx_prefill_fwd)
+    build.build()
+    dev = torch.device("cuda", 0)
+    if case == "prefill":
+        w = inputs.PREFILL_0P6B  # 256 MB of inputs and output
+        q, k, v, r = inputs.prefill_inputs_for(w, device=dev)
+        out = torch.empty_like(q)
+        fn = lambda: plx_prefill_fwd(q, k, v, r, out)  # noqa: E731
+    else:
+        if case == "decode":
+            lens = [8192] * 16  # 16 x 8192 tokens x 8 heads: 537 MB of cache
+        else:
+            lens = [1024, 40000, 3000, 17000]  # ragged, 250 MB of cache
+        dq, dr, kc, vc, sl = inputs.decode_inputs(len(lens), 16, 8, 128, lens, torch.bfloat16,
+                                                  0.05, 5, device=dev)
+        sl = sl.to(dev)
+        out = torch.empty_like(dq)
+        fn = lambda: plx_decode_fwd(dq, dr, kc, vc, sl, out)  # noqa: E731
+    for _ in range(6):
+        fn()
+    torch.cuda.synchronize(dev)
+    plx_check_device_error()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -205,9 +239,14 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 1.7B / ragged timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_ragged"], default=None,
+                    help="run 3 warm-up + 3 launches of one kernel on a profiling-sized case "
+                         "(inputs > L2, < 1 GB) and exit; prints nothing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.ncu_case:
+        return run_ncu_case(args.ncu_case)
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
@@ -264,8 +303,8 @@ def main():
     dec_ms_max = max_over_ranks(dec_ms, world, dev)
     total_ms_max = max_over_ranks(total_ms, world, dev)
     K = args.steps
-    value = world * wp.flops * K / (pre_ms_max * 1e-3) / 1e12
-    dec_gbs = world * dbytes * K / (dec_ms_max * 1e-3) / 1e9
+    value = whole_job_rate(world, wp.flops, K, pre_ms_max) / 1e12
+    dec_gbs = whole_job_rate(world, dbytes, K, dec_ms_max) / 1e9
     pre_launch_s = pre_ms / K * 1e-3
     dec_launch_s = dec_ms / K * 1e-3
     tc_peak = _peak(peaks, "bf16_tflops")
