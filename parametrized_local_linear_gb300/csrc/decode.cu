@@ -9,10 +9,13 @@
 // kernel does the same on sm_103a with warp-level mma.sync:
 //
 //   CTA (split s, kv head g, sequence b), 4 consumer warps + 1 producer warp.
-//   Producer: 1-D bulk TMA copies of the 256-byte K and V rows of its key
-//     range into a ring of shared-memory stages (row pitch 272 B, so ldmatrix
-//     is bank-conflict free), completion counted on per-stage mbarriers.
-//   Consumers: stages are dealt round-robin to the 4 warps. For each 16 keys
+//   Producer: one thread issues tiled TMA loads of 16-token x 64-dim boxes of
+//     the K and V cache (3-D tensor maps over [tokens, Hkv, d]) into a ring of
+//     8 shared-memory stages, 128-byte swizzled so ldmatrix is bank-conflict
+//     free; completion is counted in bytes on per-stage mbarriers. Four 2 KB
+//     requests move an 8 KB stage (per-row 256-byte copies were limited by
+//     the TMA request rate).
+//   Consumers: stages are dealt round-robin to the 4 warps, two per warp. For each 16 keys
 //     one m16n8k16 product gives all four dot-product families at once: A rows
 //     0..G-1 hold the G query heads' q, rows 8..8+G-1 their probes r, so the
 //     accumulator row g is the score s = q.k and row g + 8 is t = r.k for the
@@ -36,18 +39,23 @@ namespace plx {
 namespace {
 
 constexpr int D = 128;
-constexpr int KT = 32;                        // keys per stage
-constexpr int NST = 6;                        // stages in the ring
+constexpr int KT = 16;                        // keys per stage (one TMA box row count)
 constexpr int NCW = 4;                        // consumer warps
-constexpr int ROWB = D * 2 + 16;              // padded row pitch in shared memory
-constexpr int STAGE_BYTES = 2 * KT * ROWB;    // K rows then V rows
-constexpr int OFF_BAR = NST * STAGE_BYTES;    // 104448
-constexpr int SMEM_BYTES = OFF_BAR + 2 * NST * 8 + 16;
+// Tile t goes to warp t % NCW and stage t % NST. NST is a multiple of NCW, so
+// a stage is only ever consumed by one warp, which has itself consumed the
+// stage's previous phase before it waits on the next one: a parity wait can
+// never be two phases ahead (which it could not tell apart).
+constexpr int NST = 2 * NCW;                  // stages in the ring
+constexpr int HALF = KT * 128;                // one 64-dim half of KT rows, 128-byte swizzled
+constexpr int STAGE_BYTES = 4 * HALF;         // K half 0, K half 1, V half 0, V half 1
+constexpr int OFF_BAR = NST * STAGE_BYTES;    // 65536
+static_assert(NST % NCW == 0, "each stage must belong to one consumer warp");
+constexpr int SMEM_BYTES = OFF_BAR + 2 * NST * 8 + 16 + 1024;  // + alignment slack
 constexpr int REC = 2 * D + 2;                // floats per partial record
 constexpr int THREADS = 32 * (NCW + 1);
 
 struct DecodeArgs {
-  const __nv_bfloat16 *q, *r, *kc, *vc;
+  const __nv_bfloat16 *q, *r;
   const int *seqlens;
   float *ws;
   int B, Hq, Hkv, G, nsplit;
@@ -55,8 +63,18 @@ struct DecodeArgs {
   unsigned *err;
 };
 
-__global__ void __launch_bounds__(THREADS) decode_split_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+// Byte offset of 16-byte chunk c (0..15 over the 128 dims) of row `row` in a
+// stage half pair laid out by TMA with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int row, int c) {
+  return (c >> 3) * HALF + row * 128 + ((((c & 7) ^ (row & 7))) << 4);
+}
+
+__global__ void __launch_bounds__(THREADS)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *empty = full + NST;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NST);
@@ -70,10 +88,6 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const DecodeArgs 
   const int nkeys = hi - lo;
   const int ntiles = (nkeys + KT - 1) / KT;
 
-  // Zero the stages once so rows a partial last tile does not fill hold finite
-  // data (their weights are zero; 0 * finite stays 0 in the value product).
-  for (int i = threadIdx.x; i < OFF_BAR / 16; i += THREADS)
-    reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -82,43 +96,43 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const DecodeArgs 
     *abort_flag = 0;
     fence_mbar_init();
   }
-  fence_proxy_async_smem();
   __syncthreads();
   const Abort ab{abort_flag, a.err};
 
+  // Tile t covers keys [lo + KT t, min(lo + KT (t + 1), hi)). Its TMA box of KT
+  // tokens starts at token min(off + lo + KT t, off + hi - KT), so the box
+  // never reaches past the split's last key (and so never past the cache);
+  // rows in front of the tile's first key (`skip` of them: keys of the
+  // previous tile, or zero fill before token 0) are masked by the consumer.
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
     long long off = 0;
     for (int i = lane; i < b; i += 32) off += a.seqlens[i];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
-    const size_t row_pitch = static_cast<size_t>(a.Hkv) * D;  // elements between tokens
-    const __nv_bfloat16 *kbase = a.kc + (static_cast<size_t>(off + lo) * a.Hkv + kvh) * D;
-    const __nv_bfloat16 *vbase = a.vc + (static_cast<size_t>(off + lo) * a.Hkv + kvh) * D;
-    int issued = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t % NST;
-      if (t >= NST) {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(smem_u32(&empty[st]), ((t / NST) - 1) & 1, ab);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    if (lane == 0) {
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+      const int first = static_cast<int>(off) + lo, last = static_cast<int>(off) + hi;
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t % NST;
+        if (t >= NST && !mbar_wait(smem_u32(&empty[st]), ((t / NST) - 1) & 1, ab)) break;
+        const uint32_t bar = smem_u32(&full[st]);
+        mbar_arrive_expect_tx(bar, STAGE_BYTES);
+        const int z = min(first + KT * t, last - KT);
+        const uint32_t base = smem_u32(smem + st * STAGE_BYTES);
+        tma_load_3d(base, &tm_k, 0, kvh, z, bar);
+        tma_load_3d(base + HALF, &tm_k, 64, kvh, z, bar);
+        tma_load_3d(base + 2 * HALF, &tm_v, 0, kvh, z, bar);
+        tma_load_3d(base + 3 * HALF, &tm_v, 64, kvh, z, bar);
+        issued = t + 1;
       }
-      const int nvalid = min(KT, nkeys - t * KT);
-      const uint32_t bar = smem_u32(&full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nvalid) * 2u * D * 2u);
-      __syncwarp();
-      if (lane < nvalid) {
-        const size_t tok = static_cast<size_t>(t) * KT + lane;
-        const uint32_t dst = smem_u32(smem + st * STAGE_BYTES + lane * ROWB);
-        bulk_g2s(dst, kbase + tok * row_pitch, D * 2, bar);
-        bulk_g2s(dst + KT * ROWB, vbase + tok * row_pitch, D * 2, bar);
+      if (ab.raised()) {
+        // Let this thread's own copies land before the CTA exits.
+        for (int t = max(0, issued - NST); t < issued; ++t)
+          mbar_wait_drain(smem_u32(&full[t % NST]), (t / NST) & 1);
       }
-      issued = t + 1;
-    }
-    if (ab.raised() && lane == 0) {
-      // Let this warp's own copies land before the CTA exits.
-      for (int t = max(0, issued - NST); t < issued; ++t)
-        mbar_wait_drain(smem_u32(&full[t % NST]), (t / NST) & 1);
     }
   }
 
@@ -150,30 +164,30 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const DecodeArgs 
       if (lane == 0) ok = mbar_wait(smem_u32(&full[st]), (t / NST) & 1, ab);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       const uint32_t kb = smem_u32(smem + st * STAGE_BYTES);
-      const uint32_t vb = kb + KT * ROWB;
+      const uint32_t vb = kb + 2 * HALF;
+      // Rows [0, skip) of the box precede this tile's first key.
+      const int skip = (lo + KT * t) - min(lo + KT * t, hi - KT);
 #pragma unroll
       for (int half = 0; half < KT / 16; ++half) {
-        const int key0 = t * KT + half * 16;
-        if (key0 >= nkeys) break;
+        if (half * 16 + 15 < skip) continue;
         float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const uint32_t krow = kb + (half * 16 + (lane >> 4) * 8 + (lane & 7)) * ROWB +
-                              ((lane >> 3) & 1) * 16;
+        const int krow = half * 16 + (lane >> 4) * 8 + (lane & 7);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(krow + kk * 32, b0, b1, b2, b3);
+          ldsm_x4(kb + swz(krow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
           mma_bf16_16816(c[0], qa[kk], b0, b1);
           mma_bf16_16816(c[1], qa[kk], b2, b3);
         }
-        // c[n][0..1]: s for keys key0 + 8n + 2tq + {0,1}; c[n][2..3]: t for the same keys.
+        // c[n][0..1]: s for box rows half*16 + 8n + 2tq + {0,1}; c[n][2..3]: t for the same rows.
         float s[2][2];
         float mx = -INFINITY;
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int key = key0 + 8 * n + 2 * tq + e;
-            s[n][e] = key < nkeys ? c[n][e] * a.scale_log2 : -INFINITY;
+            const int row = half * 16 + 8 * n + 2 * tq + e;
+            s[n][e] = row >= skip ? c[n][e] * a.scale_log2 : -INFINITY;
             mx = fmaxf(mx, s[n][e]);
           }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -202,12 +216,11 @@ __global__ void __launch_bounds__(THREADS) decode_split_kernel(const DecodeArgs 
         }
         const uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(pt[0][0], pt[0][1]),
                                 pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(pt[1][0], pt[1][1])};
-        const uint32_t vrow = vb + (half * 16 + ((lane >> 3) & 1) * 8 + (lane & 7)) * ROWB +
-                              (lane >> 4) * 16;
+        const int vrow = half * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
         for (int nd = 0; nd < 8; ++nd) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vrow + nd * 32, b0, b1, b2, b3);
+          ldsm_x4_t(vb + swz(vrow, 2 * nd + (lane >> 4)), b0, b1, b2, b3);
           mma_bf16_16816(acc[2 * nd], pa, b0, b1);
           mma_bf16_16816(acc[2 * nd + 1], pa, b2, b3);
         }
@@ -320,11 +333,29 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return cudaErrorInvalidValue;
+  // The cache is [tokens, Hkv, d]. Its token count lives on the device, so the
+  // map declares 2^30 tokens; every box the kernel requests lies inside the
+  // tokens of its own sequence (or, for caches shorter than one box, starts
+  // at a negative token and is zero-filled there).
+  CUtensorMap mk, mv;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(1) << 30};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(Hkv) * D * 2};
+  const cuuint32_t box[3] = {64, 1, KT};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  for (int i = 0; i < 2; ++i) {
+    if (enc(i == 0 ? &mk : &mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void *>(i == 0 ? kcache : vcache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   DecodeArgs a;
   a.q = static_cast<const __nv_bfloat16 *>(q);
   a.r = static_cast<const __nv_bfloat16 *>(r);
-  a.kc = static_cast<const __nv_bfloat16 *>(kcache);
-  a.vc = static_cast<const __nv_bfloat16 *>(vcache);
   a.seqlens = seqlens;
   a.ws = workspace;
   a.B = B;
@@ -334,7 +365,7 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
   a.nsplit = nsplit;
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   a.err = err;
-  decode_split_kernel<<<dim3(nsplit, Hkv, B), THREADS, SMEM_BYTES, stream>>>(a);
+  decode_split_kernel<<<dim3(nsplit, Hkv, B), THREADS, SMEM_BYTES, stream>>>(mk, mv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<<<B * Hq, D, 0, stream>>>(workspace, static_cast<__nv_bfloat16 *>(out),
