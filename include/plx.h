@@ -108,6 +108,29 @@ plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, c
                              const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
                              int nsplit, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * plx_decode_fwd for callers that cannot allocate device memory during the
+ * call: for example code whose device memory belongs to an allocator that
+ * must not be bypassed, a host thread that must not take the driver's
+ * allocation locks, or an embedding that gives this library only its own
+ * input and output buffers. There is no counterpart in the
+ * paper; it exists for such callers only. Same arguments, layouts and results
+ * as plx_decode_fwd; the per-split records go to one fixed device array of
+ * 16 MiB that the library reserves on every device that loads it, held until
+ * the process exits. Nothing is allocated or freed by this call.
+ *   - The split count is the default one, lowered if needed so the records
+ *     fit; B * Hq * (2 d + 2) * 4 bytes (one split) must fit in 16 MiB, else
+ *     PLX_ERR_UNSUPPORTED and nothing runs.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the array: calls that overlap on the GPU race and must
+ *     be serialised by the caller. The array needs no clearing between calls
+ *     (each call writes every record it reads).
+ */
+plx_status plx_decode_fwd_noalloc(const void *q, const void *r, const void *kcache,
+                                  const void *vcache, const int *seqlens, void *out, int B, int Hq,
+                                  int Hkv, int d, void *stream);
+
 /* Bytes of decode workspace for a given split count (fp32 partials:
  * B * Hq * nsplit * (2 d + 2) * 4). */
 size_t plx_decode_workspace_bytes(int B, int Hq, int d, int nsplit);

@@ -31,6 +31,7 @@ SIGNATURES = {
     "plx_prefill_fwd_f32": (_i, [_vp] * 6 + [_i] * 5 + [_vp]),
     "plx_decode_fwd": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
     "plx_decode_fwd_ex": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
+    "plx_decode_fwd_noalloc": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
     "plx_decode_workspace_bytes": (_sz, [_i] * 4),
     "plx_decode_default_nsplit": (_i, [_i] * 2),
     "plx_check_device_error": (_i, [_vp]),
@@ -171,6 +172,24 @@ def plx_decode_fwd(q, r, kcache, vcache, seqlens, out=None, nsplit=0, workspace=
             st = L.plx_decode_fwd_ex(q.data_ptr(), r.data_ptr(), kcache.data_ptr(),
                                      vcache.data_ptr(), seqlens.data_ptr(), out.data_ptr(), B, Hq,
                                      Hkv, d, int(nsplit), ws_ptr, ws_bytes, s)
+    _check(st)
+    return out
+
+
+def plx_decode_fwd_noalloc(q, r, kcache, vcache, seqlens, out, stream=None):
+    """Decode through the entry point that allocates nothing (see include/plx.h):
+    the split records go to the library's fixed device array. ``out`` must be
+    given (bf16 [B, Hq, d]); returns it."""
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    for name, t in (("r", r), ("kcache", kcache), ("vcache", vcache), ("out", out)):
+        _need(t, name, torch.bfloat16, 3, dev)
+    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    B, Hq, d = q.shape
+    with torch.cuda.device(dev):
+        st = lib().plx_decode_fwd_noalloc(q.data_ptr(), r.data_ptr(), kcache.data_ptr(),
+                                          vcache.data_ptr(), seqlens.data_ptr(), out.data_ptr(),
+                                          B, Hq, kcache.shape[1], d, _stream(stream, dev))
     _check(st)
     return out
 

@@ -228,6 +228,29 @@ plx_status plx_decode_fwd(const void *q, const void *r, const void *kcache, cons
                            stream);
 }
 
+plx_status plx_decode_fwd_noalloc(const void *q, const void *r, const void *kcache,
+                                  const void *vcache, const int *seqlens, void *out, int B, int Hq,
+                                  int Hkv, int d, void *stream) {
+  const char *fn = "plx_decode_fwd_noalloc";
+  const size_t cap_bytes = plx::kNoAllocScratchFloats * sizeof(float);
+  int nsplit = plx_decode_default_nsplit(B, Hkv);
+  if (B >= 1 && Hq >= 1 && d >= 1) {
+    const size_t per_split = plx_decode_workspace_bytes(B, Hq, d, 1);
+    if (per_split > cap_bytes)
+      return fail(PLX_ERR_UNSUPPORTED,
+                  "%s: B * Hq = %lld needs %zu bytes of split records even with one split; "
+                  "the fixed array holds %zu bytes (use plx_decode_fwd)",
+                  fn, static_cast<long long>(B) * Hq, per_split, cap_bytes);
+    const size_t fit = cap_bytes / per_split;
+    if (static_cast<size_t>(nsplit) > fit) nsplit = static_cast<int>(fit);
+  }
+  float *scratch = nullptr;
+  cudaError_t e = plx::noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "plx_decode_fwd_noalloc: scratch address");
+  return plx_decode_fwd_ex(q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, d, nsplit, scratch,
+                           cap_bytes, stream);
+}
+
 plx_status plx_check_device_error(void *stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(st);

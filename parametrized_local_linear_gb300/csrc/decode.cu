@@ -32,6 +32,8 @@
 // per-split outputs would be wrong: O1 * s is bilinear in the partial sums.
 #include <math.h>
 
+#include <mutex>
+
 #include "plx_device.cuh"
 #include "plx_internal.h"
 
@@ -371,6 +373,43 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
   decode_combine_kernel<<<B * Hq, D, 0, stream>>>(workspace, static_cast<__nv_bfloat16 *>(out),
                                                   nsplit);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Decode without any allocation. Some callers cannot allocate device memory
+// at call time: code whose device memory belongs to an allocator that must
+// not be bypassed, a host thread that must not take the driver's allocation
+// locks, or an embedding that hands this library only its own input and
+// output buffers. For them the
+// split records live in one fixed array below, reserved when the library is
+// loaded onto a device and held by every device that loads it until the
+// process exits. Its address is resolved with cudaGetSymbolAddress once per
+// device, on the first call on that device (make that first call before any
+// stream capture). Calls that overlap on the GPU share the array and race;
+// serialise them (one stream, or events). Nothing in it needs clearing between
+// calls: each call's split kernel writes every record that its combine kernel
+// then reads.
+static __device__ __align__(256) float g_decode_noalloc_scratch[kNoAllocScratchFloats];
+
+namespace {
+std::mutex g_noalloc_mu;
+float *g_noalloc_ptr[64] = {};
+}  // namespace
+
+cudaError_t noalloc_scratch(float **ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<float *>(p);
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace plx

@@ -34,6 +34,11 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
                           const int *seqlens, void *out, int B, int Hq, int Hkv, int nsplit,
                           float *workspace, unsigned *err, cudaStream_t stream);
 
+// Fixed split-record array of the allocation-free decode: 16 MiB of fp32.
+constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;
+// Device address of that array on the current device (resolved once per device).
+cudaError_t noalloc_scratch(float **ptr);
+
 cudaError_t launch_timeout_probe(long long limit_cycles, unsigned *err, cudaStream_t stream);
 
 }  // namespace plx
