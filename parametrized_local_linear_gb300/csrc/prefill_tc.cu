@@ -11,21 +11,33 @@
 // finishes o = (O1 (1 + sigma / l) - O2) / l, i.e. o^SA - Sigma_KV rho
 // (section "Core mechanism").
 //
-// One CTA owns 128 query rows of one (batch, head); 6 warps:
-//   warp 0      TMA producer: Q and R once (128 x 128 each), then K_j, V_j
-//               (64 keys x 128) into a 3-stage ring, 128-byte swizzled.
-//   warp 1      TMEM allocator and single-thread UMMA issuer.
-//   warps 2..5  softmax / epilogue: thread = query row = TMEM lane.
+// One CTA owns 128 query rows of one (batch, head); 7 warps:
+//   warp 0      TMA producer: Q and R once (128 x 128 each), then K_j and V_j
+//               (64 keys x 128 each) into two 4-stage rings, 128-byte
+//               swizzled. A K tile is released once the S and T UMMAs that
+//               read it finish, a V tile once the value UMMAs finish.
+//   warp 1      TMEM allocator; one thread issues, per tile j, O1 += P V of
+//               tile j and then the S UMMAs of tile j + 2.
+//   warp 2      one thread issues O2 += (P o T) V of tile j and then the T
+//               UMMAs of tile j + 2.
+//   warps 3..6  softmax / epilogue: thread = query row = TMEM lane.
+// Two issuing threads, because one thread cannot issue tcgen05.mma as fast as
+// the tensor core retires these shapes (measured: 50-70 cycles per issue
+// against 48-64 cycles of work per instruction, slower still while the
+// softmax warps share the issue slots). The split keeps every ordering
+// constraint free of round trips: P(j) lives over S(j) and P o T(j) over
+// T(j), and each is overwritten by tile j + 2 from the same thread that
+// issued the UMMAs reading it (tcgen05.mma from one thread execute in order).
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,64) S_0  [64,128) T_0  [128,192) S_1  [192,256) T_1  (double buffered)
 //   [256,384) O1              [384,512) O2
-// The UMMA for tile j+1 (S, T into buffer (j+1)&1) runs while the softmax
-// warps work on tile j. The softmax writes P and P o T as packed bf16 over
-// the S columns of its buffer (S_x[0,32) = P, S_x[32,64) = P o T) and the value
-// GEMMs read them straight from TMEM (A-from-TMEM form), V from shared memory
-// (MN-major). Rescaling is lazy: the max used in the exponent only moves when
-// a row's tile max exceeds it by more than 2^8, which keeps every quantity
-// exact (they all share the stale max) and rarely touches O in TMEM.
+// The UMMAs for tile j+1 run while the softmax warps work on tile j. The
+// softmax writes P and P o T as packed bf16 (S_x[0,32) = P, T_x[0,32) =
+// P o T) and the value GEMMs read them straight from TMEM (A-from-TMEM
+// form), V from shared memory (MN-major). Rescaling is
+// lazy: the max used in the exponent only moves when a row's tile max
+// exceeds it by more than 2^8, which keeps every quantity exact (they all
+// share the stale max) and rarely touches O in TMEM.
 #include <math.h>
 
 #include "plx_device.cuh"
@@ -37,18 +49,19 @@ namespace {
 constexpr int D = 128;
 constexpr int BM = 128;                       // query rows per CTA
 constexpr int BN = 64;                        // keys per tile
-constexpr int NST = 3;                        // K/V stages
+constexpr int NST = 4;                        // stages per K / V ring
 constexpr int HALF_Q = BM * 64 * 2;           // 16 KB: 128 rows x 64 dims
 constexpr int HALF_KV = BN * 64 * 2;          // 8 KB: 64 rows x 64 dims
-constexpr int TILE_KV = 2 * HALF_KV;          // 16 KB
-constexpr int STAGE_BYTES = 2 * TILE_KV;      // K then V
+constexpr int TILE_KV = 2 * HALF_KV;          // 16 KB: one K or V tile
 constexpr int OFF_Q = 0;
 constexpr int OFF_R = 2 * HALF_Q;
-constexpr int OFF_KV = 4 * HALF_Q;            // 65536
-constexpr int OFF_BAR = OFF_KV + NST * STAGE_BYTES;  // 163840
-constexpr int NBAR = 1 + 2 * NST + 2 + 2 + 1 + 1;
+constexpr int OFF_K = 4 * HALF_Q;             // 65536
+constexpr int OFF_V = OFF_K + NST * TILE_KV;  // 131072
+constexpr int OFF_BAR = OFF_V + NST * TILE_KV;  // 196608
+constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 2;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
-constexpr int THREADS = 192;
+constexpr int SM_WARP0 = 3;                   // first softmax warp
+constexpr int THREADS = 32 * (SM_WARP0 + 4);
 constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_T = 64, COL_O1 = 256, COL_O2 = 384;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
@@ -72,12 +85,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                               ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *q_full = bars;
-  uint64_t *kv_full = bars + 1;
-  uint64_t *kv_empty = bars + 1 + NST;
-  uint64_t *st_full = bars + 1 + 2 * NST;
-  uint64_t *p_full = st_full + 2;
-  uint64_t *pv_done = p_full + 2;
-  uint64_t *mma_drain = pv_done + 1;
+  uint64_t *k_full = bars + 1;
+  uint64_t *k_empty = k_full + NST;
+  uint64_t *v_full = k_empty + NST;
+  uint64_t *v_empty = v_full + NST;
+  uint64_t *st_full = v_empty + NST;   // [2]
+  uint64_t *p_full = st_full + 2;      // [2]
+  uint64_t *pv_done = p_full + 2;      // [2]: value UMMAs of the tiles using buffer x
+  uint64_t *drain = pv_done + 2;       // [2]: one per issuing thread
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -96,15 +111,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
     for (int s = 0; s < NST; ++s) {
-      mbar_init(smem_u32(&kv_full[s]), 1);
-      mbar_init(smem_u32(&kv_empty[s]), 1);
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 2);
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 2);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(smem_u32(&st_full[x]), 1);
+      mbar_init(smem_u32(&st_full[x]), 2);
       mbar_init(smem_u32(&p_full[x]), 128);
+      mbar_init(smem_u32(&pv_done[x]), 2);
+      mbar_init(smem_u32(&drain[x]), 1);
     }
-    mbar_init(smem_u32(pv_done), 1);
-    mbar_init(smem_u32(mma_drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -134,79 +151,86 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_load_3d(smem_u32(smem + OFF_Q + HALF_Q), &tm_q, 64, q0, zq, qb);
       tma_load_3d(smem_u32(smem + OFF_R), &tm_r, 0, q0, zq, qb);
       tma_load_3d(smem_u32(smem + OFF_R + HALF_Q), &tm_r, 64, q0, zq, qb);
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % NST;
-        if (j >= NST && !mbar_wait(smem_u32(&kv_empty[st]), ((j / NST) - 1) & 1, ab)) break;
-        const uint32_t fb = smem_u32(&kv_full[st]);
-        mbar_arrive_expect_tx(fb, STAGE_BYTES);
-        const uint32_t base = smem_u32(smem + OFF_KV + st * STAGE_BYTES);
-        tma_load_3d(base, &tm_k, 0, j * BN, zk, fb);
-        tma_load_3d(base + HALF_KV, &tm_k, 64, j * BN, zk, fb);
-        tma_load_3d(base + TILE_KV, &tm_v, 0, j * BN, zk, fb);
-        tma_load_3d(base + TILE_KV + HALF_KV, &tm_v, 64, j * BN, zk, fb);
-        issued = j + 1;
+        if (j >= NST && !mbar_wait(smem_u32(&k_empty[st]), ((j / NST) - 1) & 1, ab)) break;
+        const uint32_t kf = smem_u32(&k_full[st]);
+        mbar_arrive_expect_tx(kf, TILE_KV);
+        const uint32_t kb = smem_u32(smem + OFF_K + st * TILE_KV);
+        tma_load_3d(kb, &tm_k, 0, j * BN, zk, kf);
+        tma_load_3d(kb + HALF_KV, &tm_k, 64, j * BN, zk, kf);
+        k_issued = j + 1;
+        if (j >= NST && !mbar_wait(smem_u32(&v_empty[st]), ((j / NST) - 1) & 1, ab)) break;
+        const uint32_t vf = smem_u32(&v_full[st]);
+        mbar_arrive_expect_tx(vf, TILE_KV);
+        const uint32_t vb = smem_u32(smem + OFF_V + st * TILE_KV);
+        tma_load_3d(vb, &tm_v, 0, j * BN, zk, vf);
+        tma_load_3d(vb + HALF_KV, &tm_v, 64, j * BN, zk, vf);
+        v_issued = j + 1;
       }
       if (ab.raised()) {
+        // Let this thread's own copies land before the CTA exits.
         mbar_wait_drain(qb, 0);
-        for (int j = max(0, issued - NST); j < issued; ++j)
-          mbar_wait_drain(smem_u32(&kv_full[j % NST]), (j / NST) & 1);
+        for (int j = max(0, k_issued - NST); j < k_issued; ++j)
+          mbar_wait_drain(smem_u32(&k_full[j % NST]), (j / NST) & 1);
+        for (int j = max(0, v_issued - NST); j < v_issued; ++j)
+          mbar_wait_drain(smem_u32(&v_full[j % NST]), (j / NST) & 1);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
-      // ---------------------------------------------------------- UMMA issuer
+      // ---------------------------------------------------------- UMMA issuers
+      // Thread 1 (warp 1): O1 += P V of tile j, then S of tile j + 2.
+      // Thread 2 (warp 2): O2 += (P o T) V of tile j, then T of tile j + 2.
+      // Each commits its half of st_full, k_empty, pv_done and v_empty
+      // (count 2). Descriptors are built once; a K step only adds
+      // a constant to the start-address field (16-byte units, never carrying
+      // out of its 14 bits since shared memory is below 256 KB).
+      const bool is_s = warp == 1;
       constexpr uint32_t idesc_st = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
-      const uint32_t sq = smem_u32(smem + OFF_Q), sr = smem_u32(smem + OFF_R);
-      auto issue_st = [&](int j) -> bool {
-        const int st = j % NST;
-        if (!mbar_wait(smem_u32(&kv_full[st]), (j / NST) & 1, ab)) return false;
+      const uint64_t adesc = smem_desc_sw128(smem_u32(smem + (is_s ? OFF_Q : OFF_R)), 16, 1024);
+      const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
+      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + OFF_V), HALF_KV, 1024);
+      const uint32_t col_off = is_s ? 0u : COL_T;
+      auto issue_scores = [&](int j) -> bool {  // S or T of tile j
+        const int x = j & 1, st = j % NST;
+        if (!mbar_wait(smem_u32(&k_full[st]), (j / NST) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t kb = smem_u32(smem + OFF_KV + st * STAGE_BYTES);
-        const uint32_t cs = tbase + ((j & 1) ? COL_S1 : COL_S0);
+        const uint64_t kdesc = kdesc0 + st * (TILE_KV >> 4);
+        const uint32_t d = tbase + (x ? COL_S1 : COL_S0) + col_off;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t qo = (ks >> 2) * HALF_Q + (ks & 3) * 32;
-          const uint32_t ko = (ks >> 2) * HALF_KV + (ks & 3) * 32;
-          umma_ss(cs, smem_desc_sw128(sq + qo, 16, 1024), smem_desc_sw128(kb + ko, 16, 1024),
-                  idesc_st, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t qo = (ks >> 2) * HALF_Q + (ks & 3) * 32;
-          const uint32_t ko = (ks >> 2) * HALF_KV + (ks & 3) * 32;
-          umma_ss(cs + COL_T, smem_desc_sw128(sr + qo, 16, 1024),
-                  smem_desc_sw128(kb + ko, 16, 1024), idesc_st, ks > 0);
-        }
-        umma_commit(smem_u32(&st_full[j & 1]));
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(d, adesc + (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2,
+                  kdesc + (ks >> 2) * (HALF_KV >> 4) + (ks & 3) * 2, idesc_st, ks > 0);
+        umma_commit(smem_u32(&st_full[x]));
+        umma_commit(smem_u32(&k_empty[st]));
         return true;
       };
       bool ok = mbar_wait(smem_u32(q_full), 0, ab);
       if (ok) {
         tc_fence_after();
-        ok = issue_st(0);
+        ok = issue_scores(0) && (ntiles < 2 || issue_scores(1));
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        if (j + 1 < ntiles && !issue_st(j + 1)) break;
-        if (!mbar_wait(smem_u32(&p_full[j & 1]), (j >> 1) & 1, ab)) break;
+        const int x = j & 1, st = j % NST;
+        if (!mbar_wait(smem_u32(&p_full[x]), (j >> 1) & 1, ab)) break;
+        if (!mbar_wait(smem_u32(&v_full[st]), (j / NST) & 1, ab)) break;
         tc_fence_after();
-        const uint32_t vb = smem_u32(smem + OFF_KV + (j % NST) * STAGE_BYTES + TILE_KV);
-        const uint32_t cp = tbase + ((j & 1) ? COL_S1 : COL_S0);
+        const uint64_t vdesc = vdesc0 + st * (TILE_KV >> 4);
+        const uint32_t ap = tbase + (x ? COL_S1 : COL_S0) + col_off;  // P or P o T
+        const uint32_t dout = tbase + (is_s ? COL_O1 : COL_O2);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
-          umma_ts(tbase + COL_O1, cp + ks * 8, smem_desc_sw128(vb + ks * 2048, HALF_KV, 1024),
-                  idesc_pv, (j > 0 || ks > 0));
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          umma_ts(tbase + COL_O2, cp + 32 + ks * 8, smem_desc_sw128(vb + ks * 2048, HALF_KV, 1024),
-                  idesc_pv, (j > 0 || ks > 0));
-        umma_commit(smem_u32(pv_done));
-        umma_commit(smem_u32(&kv_empty[j % NST]));
+          umma_ts(dout, ap + ks * 8, vdesc + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0));
+        umma_commit(smem_u32(&pv_done[x]));
+        umma_commit(smem_u32(&v_empty[st]));
+        if (j + 2 < ntiles && !issue_scores(j + 2)) break;
       }
       // Every UMMA this thread issued must finish before TMEM is released.
-      umma_commit(smem_u32(mma_drain));
-      mbar_wait_drain(smem_u32(mma_drain), 0);
+      umma_commit(smem_u32(&drain[is_s ? 0 : 1]));
+      mbar_wait_drain(smem_u32(&drain[is_s ? 0 : 1]), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -223,21 +247,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const uint32_t cs = tl + (x ? COL_S1 : COL_S0);
-      float s[64], t[64];
+      float s[64];
       tmem_ld32(cs, *reinterpret_cast<float(*)[32]>(&s[0]));
       tmem_ld32(cs + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
-      tmem_ld32(cs + COL_T, *reinterpret_cast<float(*)[32]>(&t[0]));
-      tmem_ld32(cs + COL_T + 32, *reinterpret_cast<float(*)[32]>(&t[32]));
       tmem_wait_ld();
       if (j * BN + BN - 1 > q0) {  // tile reaches the diagonal: causal mask
 #pragma unroll
         for (int e = 0; e < BN; ++e)
           if (j * BN + e > grow) s[e] = -INFINITY;
       }
-      float mt = -INFINITY;
+      // Row max as 8 independent chains and a tree.
+      float mx8[8];
 #pragma unroll
-      for (int e = 0; e < BN; ++e) mt = fmaxf(mt, s[e]);
-      mt *= c;
+      for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+#pragma unroll
+      for (int e = 8; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], s[e]);
+#pragma unroll
+      for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w]);
+      const float mt = mx8[0] * c;
       const bool need = mt > m_used + kRescaleThreshold;
       float alpha = 1.f;
       if (need) {
@@ -247,26 +276,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         m_used = mt;
       }
       const float msub = m_used == -INFINITY ? 0.f : m_used;
-      uint32_t pk[32], ptk[32];
+      float lp[4] = {0.f, 0.f, 0.f, 0.f}, sp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < BN; e += 2) {
-        const float p0 = fast_exp2(fmaf(s[e], c, -msub));
-        const float p1 = fast_exp2(fmaf(s[e + 1], c, -msub));
-        const float pt0 = p0 * t[e], pt1 = p1 * t[e + 1];
-        l += p0 + p1;
-        sg += pt0 + pt1;
-        pk[e >> 1] = pack_bf16x2(p0, p1);
-        ptk[e >> 1] = pack_bf16x2(pt0, pt1);
+      for (int hf = 0; hf < 2; ++hf) {
+        // S is all in registers, so P may now overwrite it in TMEM.
+        float t[32];
+        tmem_ld32(cs + COL_T + 32 * hf, t);
+        tmem_wait_ld();
+        uint32_t pk[16], ptk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = fast_exp2(fmaf(s[32 * hf + e], c, -msub));
+          const float p1 = fast_exp2(fmaf(s[32 * hf + e + 1], c, -msub));
+          const float pt0 = p0 * t[e], pt1 = p1 * t[e + 1];
+          lp[(e >> 1) & 3] += p0 + p1;
+          sp[(e >> 1) & 3] += pt0 + pt1;
+          pk[e >> 1] = pack_bf16x2(p0, p1);
+          ptk[e >> 1] = pack_bf16x2(pt0, pt1);
+        }
+        tmem_st16(cs + 16 * hf, pk);
+        tmem_st16(cs + COL_T + 16 * hf, ptk);  // T[0,32) was read in half 0
       }
-      tmem_st16(cs, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-      tmem_st16(cs + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-      tmem_st16(cs + 32, *reinterpret_cast<uint32_t(*)[16]>(&ptk[0]));
-      tmem_st16(cs + 48, *reinterpret_cast<uint32_t(*)[16]>(&ptk[16]));
+      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+      sg += (sp[0] + sp[1]) + (sp[2] + sp[3]);
       tmem_wait_st();
       if (j > 0) {
-        // The previous tile's value GEMMs must be done before O is touched
+        // The previous tile's value UMMAs must be done before O is touched
         // and before P of this tile is handed over.
-        ok = mbar_wait(smem_u32(pv_done), (j - 1) & 1, ab);
+        ok = mbar_wait(smem_u32(&pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, ab);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, need)) {
@@ -287,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(smem_u32(&p_full[x]));
     }
     if (ok) {
-      ok = mbar_wait(smem_u32(pv_done), (ntiles - 1) & 1, ab);
+      ok = mbar_wait(smem_u32(&pv_done[(ntiles - 1) & 1]), ((ntiles - 1) >> 1) & 1, ab);
       ok = __all_sync(0xffffffffu, ok);
     }
     uint8_t *so = smem + OFF_Q;  // Q is dead once every UMMA has finished
@@ -318,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       fence_proxy_async_smem();
     }
     named_bar_sync(1, 128);
-    if (warp == 2 && lane == 0 && !ab.raised()) {
+    if (warp == SM_WARP0 && lane == 0 && !ab.raised()) {
       tma_store_3d(&tm_o, smem_u32(so), 0, q0, zq);
       tma_store_3d(&tm_o, smem_u32(so + HALF_Q), 64, q0, zq);
       bulk_commit_group();
