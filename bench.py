@@ -37,9 +37,11 @@ from parametrized_local_linear_gb300 import inputs  # noqa: E402
 
 METRIC = "Parallax fwd: prefill TFLOP/s, decode HBM GB/s; % of GB300 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu
-# summaries under profiles/ (None until captured for the current kernel).
-NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": None, "decode_split_kernel": None}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch, from the ncu
+# captures summarised in profiles/ (prefill: the bench's own workload;
+# decode: a quarter-size batch scaled by 4, the traffic being proportional to
+# the cache streamed). Set to None whenever a kernel changes after its capture.
+NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": 391.4e6, "decode_split_kernel": 4 * 548.5e6}
 
 
 def load_peaks():
