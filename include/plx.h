@@ -136,8 +136,8 @@ plx_status plx_decode_fwd_noalloc(const void *q, const void *r, const void *kcac
 size_t plx_decode_workspace_bytes(int B, int Hq, int d, int nsplit);
 
 /* The split count plx_decode_fwd uses on the current device for B sequences
- * of Hkv KV heads (targets a few CTAs per SM; lengths are not known on the
- * host). */
+ * of Hkv KV heads: about 12 CTAs per SM in total, at most 256 splits
+ * (lengths are on the device, so the host does not look at them). */
 int plx_decode_default_nsplit(int B, int Hkv);
 
 /* Synchronises `stream`, then reads and clears the device error word.
