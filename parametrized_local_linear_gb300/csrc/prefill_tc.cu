@@ -11,23 +11,23 @@
 // finishes o = (O1 (1 + sigma / l) - O2) / l, i.e. o^SA - Sigma_KV rho
 // (section "Core mechanism").
 //
-// One CTA owns 128 query rows of one (batch, head); 7 warps:
+// One CTA owns 128 query rows of one (batch, head); 9 warps:
 //   warp 0      TMA producer: Q and R once (128 x 128 each), then K_j and V_j
 //               (64 keys x 128 each) into two 4-stage rings, 128-byte
 //               swizzled. A K tile is released once the S and T UMMAs that
 //               read it finish, a V tile once the value UMMAs finish.
-//   warp 1      TMEM allocator; one thread issues, per tile j, O1 += P V of
-//               tile j and then the S UMMAs of tile j + 2.
-//   warp 2      one thread issues O2 += (P o T) V of tile j and then the T
-//               UMMAs of tile j + 2.
+//   warp 1      TMEM allocator; one thread issues O1 += P V.
+//   warp 2      one thread issues O2 += (P o T) V.
 //   warps 3..6  softmax / epilogue: thread = query row = TMEM lane.
-// Two issuing threads, because one thread cannot issue tcgen05.mma as fast as
-// the tensor core retires these shapes (measured: 50-70 cycles per issue
-// against 48-64 cycles of work per instruction, slower still while the
-// softmax warps share the issue slots). The split keeps every ordering
-// constraint free of round trips: P(j) lives over S(j) and P o T(j) over
-// T(j), and each is overwritten by tile j + 2 from the same thread that
-// issued the UMMAs reading it (tcgen05.mma from one thread execute in order).
+//   warp 7      one thread issues S = Q K^T.
+//   warp 8      one thread issues T = R K^T.
+// Four issuing threads, because one thread cannot issue tcgen05.mma as fast
+// as the tensor core retires these shapes (measured: 50-100 cycles per issue
+// under load against 48-64 cycles of work per instruction). The value UMMAs,
+// which sit on the critical path (softmax -> P V -> next softmax), have
+// issuers of their own that respond at once; S and T of tile j + 2 overwrite
+// P(j) and P o T(j) and therefore wait for the value UMMAs of tile j
+// (pv_done), which leaves them two tiles of slack.
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,64) S_0  [64,128) T_0  [128,192) S_1  [192,256) T_1  (double buffered)
 //   [256,384) O1              [384,512) O2
@@ -58,10 +58,10 @@ constexpr int OFF_R = 2 * HALF_Q;
 constexpr int OFF_K = 4 * HALF_Q;             // 65536
 constexpr int OFF_V = OFF_K + NST * TILE_KV;  // 131072
 constexpr int OFF_BAR = OFF_V + NST * TILE_KV;  // 196608
-constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 2;
+constexpr int NBAR = 1 + 4 * NST + 2 + 2 + 2 + 4;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
 constexpr int SM_WARP0 = 3;                   // first softmax warp
-constexpr int THREADS = 32 * (SM_WARP0 + 4);
+constexpr int THREADS = 32 * 9;
 constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_T = 64, COL_O1 = 256, COL_O2 = 384;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *st_full = v_empty + NST;   // [2]
   uint64_t *p_full = st_full + 2;      // [2]
   uint64_t *pv_done = p_full + 2;      // [2]: value UMMAs of the tiles using buffer x
-  uint64_t *drain = pv_done + 2;       // [2]: one per issuing thread
+  uint64_t *drain = pv_done + 2;       // [4]: one per issuing thread
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -120,8 +120,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&st_full[x]), 2);
       mbar_init(smem_u32(&p_full[x]), 128);
       mbar_init(smem_u32(&pv_done[x]), 2);
-      mbar_init(smem_u32(&drain[x]), 1);
     }
+    for (int x = 0; x < 4; ++x) mbar_init(smem_u32(&drain[x]), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -180,23 +180,47 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
-      // ---------------------------------------------------------- UMMA issuers
-      // Thread 1 (warp 1): O1 += P V of tile j, then S of tile j + 2.
-      // Thread 2 (warp 2): O2 += (P o T) V of tile j, then T of tile j + 2.
-      // Each commits its half of st_full, k_empty, pv_done and v_empty
-      // (count 2). Descriptors are built once; a K step only adds
-      // a constant to the start-address field (16-byte units, never carrying
-      // out of its 14 bits since shared memory is below 256 KB).
-      const bool is_s = warp == 1;
-      constexpr uint32_t idesc_st = idesc_bf16_f32(BM, BN, 0);
+      // ---------------------------------------------------------- value UMMAs
+      // Warp 1: O1 += P V (P over S); warp 2: O2 += (P o T) V (over T).
+      const bool is_o1 = warp == 1;
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, 1);
+      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + OFF_V), HALF_KV, 1024);
+      const uint32_t col_off = is_o1 ? 0u : COL_T;
+      const uint32_t dout = tbase + (is_o1 ? COL_O1 : COL_O2);
+      for (int j = 0; j < ntiles; ++j) {
+        const int x = j & 1, st = j % NST;
+        if (!mbar_wait(smem_u32(&p_full[x]), (j >> 1) & 1, ab)) break;
+        if (!mbar_wait(smem_u32(&v_full[st]), (j / NST) & 1, ab)) break;
+        tc_fence_after();
+        const uint64_t vdesc = vdesc0 + st * (TILE_KV >> 4);
+        const uint32_t ap = tbase + (x ? COL_S1 : COL_S0) + col_off;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          umma_ts(dout, ap + ks * 8, vdesc + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0));
+        umma_commit(smem_u32(&pv_done[x]));
+        umma_commit(smem_u32(&v_empty[st]));
+      }
+      // Every UMMA this thread issued must finish before TMEM is released.
+      umma_commit(smem_u32(&drain[is_o1 ? 0 : 1]));
+      mbar_wait_drain(smem_u32(&drain[is_o1 ? 0 : 1]), 0);
+    }
+  } else if (warp == 7 || warp == 8) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- score UMMAs
+      // Warp 7: S = Q K^T; warp 8: T = R K^T. Descriptors are built once; a K
+      // step only adds a constant to the start-address field (16-byte units,
+      // never carrying out of its 14 bits since shared memory is below 256 KB).
+      const bool is_s = warp == 7;
+      constexpr uint32_t idesc_st = idesc_bf16_f32(BM, BN, 0);
       const uint64_t adesc = smem_desc_sw128(smem_u32(smem + (is_s ? OFF_Q : OFF_R)), 16, 1024);
       const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
-      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + OFF_V), HALF_KV, 1024);
       const uint32_t col_off = is_s ? 0u : COL_T;
-      auto issue_scores = [&](int j) -> bool {  // S or T of tile j
+      bool ok = mbar_wait(smem_u32(q_full), 0, ab);
+      for (int j = 0; ok && j < ntiles; ++j) {
         const int x = j & 1, st = j % NST;
-        if (!mbar_wait(smem_u32(&k_full[st]), (j / NST) & 1, ab)) return false;
+        // Buffer x still holds P / P o T of tile j - 2 until its value UMMAs finish.
+        if (j >= 2 && !mbar_wait(smem_u32(&pv_done[x]), ((j - 2) >> 1) & 1, ab)) break;
+        if (!mbar_wait(smem_u32(&k_full[st]), (j / NST) & 1, ab)) break;
         tc_fence_after();
         const uint64_t kdesc = kdesc0 + st * (TILE_KV >> 4);
         const uint32_t d = tbase + (x ? COL_S1 : COL_S0) + col_off;
@@ -206,33 +230,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                   kdesc + (ks >> 2) * (HALF_KV >> 4) + (ks & 3) * 2, idesc_st, ks > 0);
         umma_commit(smem_u32(&st_full[x]));
         umma_commit(smem_u32(&k_empty[st]));
-        return true;
-      };
-      bool ok = mbar_wait(smem_u32(q_full), 0, ab);
-      if (ok) {
-        tc_fence_after();
-        ok = issue_scores(0) && (ntiles < 2 || issue_scores(1));
       }
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int x = j & 1, st = j % NST;
-        if (!mbar_wait(smem_u32(&p_full[x]), (j >> 1) & 1, ab)) break;
-        if (!mbar_wait(smem_u32(&v_full[st]), (j / NST) & 1, ab)) break;
-        tc_fence_after();
-        const uint64_t vdesc = vdesc0 + st * (TILE_KV >> 4);
-        const uint32_t ap = tbase + (x ? COL_S1 : COL_S0) + col_off;  // P or P o T
-        const uint32_t dout = tbase + (is_s ? COL_O1 : COL_O2);
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          umma_ts(dout, ap + ks * 8, vdesc + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0));
-        umma_commit(smem_u32(&pv_done[x]));
-        umma_commit(smem_u32(&v_empty[st]));
-        if (j + 2 < ntiles && !issue_scores(j + 2)) break;
-      }
-      // Every UMMA this thread issued must finish before TMEM is released.
-      umma_commit(smem_u32(&drain[is_s ? 0 : 1]));
-      mbar_wait_drain(smem_u32(&drain[is_s ? 0 : 1]), 0);
+      umma_commit(smem_u32(&drain[is_s ? 2 : 3]));
+      mbar_wait_drain(smem_u32(&drain[is_s ? 2 : 3]), 0);
     }
-  } else {
+  } else if (warp >= SM_WARP0 && warp < SM_WARP0 + 4) {
     // ------------------------------------------------------------ softmax
     const int qw = warp & 3;             // TMEM lane quarter this warp may touch
     const int row = qw * 32 + lane;      // query row within the tile
