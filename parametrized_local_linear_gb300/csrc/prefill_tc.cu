@@ -258,17 +258,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int e = 0; e < BN; ++e)
           if (j * BN + e > grow) s[e] = -INFINITY;
       }
-      // Row max as 8 independent chains and a tree.
+      // Row max: 8 independent chains of 3-input max, then a tree.
       float mx8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = s[e];
+      for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(s[2 * e], s[2 * e + 1]);
 #pragma unroll
-      for (int e = 8; e < BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], s[e]);
-#pragma unroll
-      for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-        for (int e = 0; e < w; ++e) mx8[e] = fmaxf(mx8[e], mx8[e + w]);
-      const float mt = mx8[0] * c;
+      for (int e = 16; e < BN; e += 2) mx8[(e >> 1) & 7] = fmax3(mx8[(e >> 1) & 7], s[e], s[e + 1]);
+      const float mt =
+          fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * c;
       const bool need = mt > m_used + kRescaleThreshold;
       float alpha = 1.f;
       if (need) {
@@ -278,7 +275,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         m_used = mt;
       }
       const float msub = m_used == -INFINITY ? 0.f : m_used;
-      float lp[4] = {0.f, 0.f, 0.f, 0.f}, sp[4] = {0.f, 0.f, 0.f, 0.f};
+      // Pairs of columns in packed fp32; one pair in four takes its
+      // exponentials from the FMA-pipe polynomial, the rest from MUFU, which
+      // balances the two units (MUFU alone was the softmax's bottleneck).
+      const uint64_t c2 = f2(c, c), nm2 = f2(-msub, -msub);
+      uint64_t lp[2] = {f2(0.f, 0.f), f2(0.f, 0.f)}, sp[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         // S is all in registers, so P may now overwrite it in TMEM.
@@ -288,19 +289,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t pk[16], ptk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = fast_exp2(fmaf(s[32 * hf + e], c, -msub));
-          const float p1 = fast_exp2(fmaf(s[32 * hf + e + 1], c, -msub));
-          const float pt0 = p0 * t[e], pt1 = p1 * t[e + 1];
-          lp[(e >> 1) & 3] += p0 + p1;
-          sp[(e >> 1) & 3] += pt0 + pt1;
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-          ptk[e >> 1] = pack_bf16x2(pt0, pt1);
+          const uint64_t x = ffma2(f2(s[32 * hf + e], s[32 * hf + e + 1]), c2, nm2);
+          const uint64_t p = ((e >> 1) & 3) == 3 ? exp2_poly2(x)
+                                                 : f2(fast_exp2(f2lo(x)), fast_exp2(f2hi(x)));
+          const uint64_t pt = fmul2(p, f2(t[e], t[e + 1]));
+          lp[(e >> 1) & 1] = fadd2(lp[(e >> 1) & 1], p);
+          sp[(e >> 1) & 1] = fadd2(sp[(e >> 1) & 1], pt);
+          pk[e >> 1] = pack_bf16x2(p);
+          ptk[e >> 1] = pack_bf16x2(pt);
         }
         tmem_st16(cs + 16 * hf, pk);
         tmem_st16(cs + COL_T + 16 * hf, ptk);  // T[0,32) was read in half 0
       }
-      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
-      sg += (sp[0] + sp[1]) + (sp[2] + sp[3]);
+      const uint64_t lsum = fadd2(lp[0], lp[1]), ssum = fadd2(sp[0], sp[1]);
+      l += f2lo(lsum) + f2hi(lsum);
+      sg += f2lo(ssum) + f2hi(ssum);
       tmem_wait_st();
       if (j > 0) {
         // The previous tile's value UMMAs must be done before O is touched
