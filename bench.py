@@ -75,7 +75,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -235,7 +235,7 @@ def run_ncu_case(case):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="plx", choices=["plx", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the 1.7B / ragged timings")
@@ -289,7 +289,12 @@ def main():
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        time.sleep(0.3)  # let the sampler start
+        # Keep the GPU busy while the sampler starts, so its samples are taken
+        # under load; these steps are not timed.
+        t_end = time.time() + 0.6
+        while time.time() < t_end:
+            step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+            torch.cuda.synchronize(dev)
         t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for i in range(args.steps):
