@@ -12,7 +12,9 @@ section "Core mechanism", output equation). This module compiles that file
 with gcc, loads it with ctypes and walks the (batch, head, row) index space:
 
 * ``prefill``: causal -- query i of head h sees keys 0..i of KV head h // G,
-  G = Hq / Hkv (consecutive grouping, the plainest GQA reading).
+  G = Hq / Hkv (consecutive grouping, the plainest GQA reading); with more
+  keys than queries the queries are the last positions (a chunk appended to
+  a cache) and query i sees keys 0 .. Lk - L + i.
 * ``decode``: one query per (sequence, head) sees all ``seqlens[b]`` cached
   keys; the cache is packed ``[sum(seqlens), Hkv, d]``.
 
@@ -123,13 +125,17 @@ def _rows(nkeys, Q, R, K, V, tau):
 def prefill(q, k, v, r, rows=None, threads=None):
     """Causal Parallax prefill.
 
-    q, r: [B, Hq, L, d]; k, v: [B, Hkv, L, d]. ``rows`` is None (every row) or
-    an iterable of (b, h, i). Returns (out, lse): with rows=None, out is
-    [B, Hq, L, d] and lse [B, Hq, L]; otherwise out is [n, d], lse [n] in the
-    order of ``rows``.
+    q, r: [B, Hq, L, d]; k, v: [B, Hkv, Lk, d] with Lk >= L. The L queries are
+    the last L of the Lk positions, so query i sees keys 0 .. Lk - L + i
+    (Lk == L: ordinary causal prefill; Lk > L: a chunk appended to an existing
+    cache). ``rows`` is None (every row) or an iterable of (b, h, i). Returns
+    (out, lse): with rows=None, out is [B, Hq, L, d] and lse [B, Hq, L];
+    otherwise out is [n, d], lse [n] in the order of ``rows``.
     """
     B, Hq, L, d = q.shape
     Hkv = k.shape[1]
+    offset = k.shape[2] - L
+    assert offset >= 0
     assert Hq % Hkv == 0
     G = Hq // Hkv
     tau = 1.0 / math.sqrt(d)
@@ -150,7 +156,7 @@ def prefill(q, k, v, r, rows=None, threads=None):
         idx = np.array([i for _, i in items])
         Kb = _f64(k[b, h // G]); Vb = _f64(v[b, h // G])
         Qb = _f64(q[b, h])[idx]; Rb = _f64(r[b, h])[idx]
-        o, l = _rows(idx + 1, Qb, Rb, Kb, Vb, tau)
+        o, l = _rows(offset + idx + 1, Qb, Rb, Kb, Vb, tau)
         for (n, _), on, ln in zip(items, o, l):
             out[n] = on; lse[n] = ln
 

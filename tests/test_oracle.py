@@ -245,3 +245,14 @@ def test_row_sampling_matches_full_pass():
     o, l = oracle.prefill(q, k, v, r, rows=rows)
     for n, (b, h, i) in enumerate(rows):
         assert np.array_equal(o[n], full[b, h, i]) and l[n] == flse[b, h, i]
+
+
+def test_chunked_prefill_is_the_tail_of_the_full_prefill():
+    """A chunk of Lq queries over Lk keys (query i sees keys 0..Lk-Lq+i) is the
+    last Lq rows of the full causal prefill over the same keys."""
+    q, k, v, r = _small(B=1, Hq=4, Hkv=2, L=40, d=8, seed=41)
+    full, flse = oracle.prefill(q, k, v, r)
+    for lq in (1, 7, 40):
+        out, lse = oracle.prefill(q[:, :, -lq:].contiguous(), k, v, r[:, :, -lq:].contiguous())
+        np.testing.assert_array_equal(out, full[:, :, -lq:])
+        np.testing.assert_array_equal(lse, flse[:, :, -lq:])
