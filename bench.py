@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # captures summarised in profiles/ (prefill: the bench's own workload;
 # decode: a quarter-size batch scaled by 4, the traffic being proportional to
 # the cache streamed). Set to None whenever a kernel changes after its capture.
-NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": 381.8e6, "decode_split_kernel": 4 * 543.9e6}
+NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": None, "decode_split_kernel": 4 * 543.9e6}
 
 
 def load_peaks():
@@ -370,7 +370,26 @@ def main():
         t3 = a.elapsed_time(b) / n3 * 1e-3
         extra[w3.name] = {"value": w3.flops / t3 / 1e12, "unit": "TFLOP/s", "ms": t3 * 1e3,
                           "frac_of_peak": w3.flops / t3 / 1e12 / tc_peak}
-        del q3, k3, v3, r3, o3
+        # Chunked prefill: the last 2048 positions of a 16384-token sequence
+        # (a new chunk against an existing cache), 1.7B-shaped heads.
+        from parametrized_local_linear_gb300 import plx_prefill_fwd_chunk
+        lq = 2048
+        qc, rc = q3[:, :, -lq:].contiguous(), r3[:, :, -lq:].contiguous()
+        oc = torch.empty_like(qc)
+        for _ in range(3):
+            plx_prefill_fwd_chunk(qc, k3, v3, rc, oc)
+        a.record(stream)
+        for _ in range(n3):
+            plx_prefill_fwd_chunk(qc, k3, v3, rc, oc)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        tc = a.elapsed_time(b) / n3 * 1e-3
+        lk = w3.L
+        cflops = 8 * w3.d * w3.B * w3.Hq * (lq * (lk - lq) + lq * (lq + 1) // 2)
+        extra["prefill_chunk_Lq2048_Lk16384_B1_Hq16_Hkv8_d128"] = {
+            "value": cflops / tc / 1e12, "unit": "TFLOP/s", "ms": tc * 1e3,
+            "frac_of_peak": cflops / tc / 1e12 / tc_peak}
+        del q3, k3, v3, r3, o3, qc, rc, oc
         w5 = inputs.DECODE_RAGGED
         d5 = inputs.decode_inputs_for(w5, device=dev)
         sl5 = d5[4].to(dev)

@@ -69,6 +69,20 @@ plx_status plx_prefill_fwd(const void *q, const void *k, const void *v, const vo
                            void *stream);
 
 /*
+ * Chunked causal prefill: Lq new queries against Lk >= Lq keys of which they
+ * are the last Lq positions (a chunk appended to an existing cache, the
+ * cache already holding the chunk's own keys). Query row i sees keys
+ * 0 .. Lk - Lq + i. Same dtypes and rules as plx_prefill_fwd; layouts:
+ *   q, r, out : bf16 [B, Hq, Lq, d];   k, v : bf16 [B, Hkv, Lk, d];
+ *   lse       : fp32 [B, Hq, Lq] or NULL.
+ * plx_prefill_fwd is this call with Lq = Lk = L. The pages do not describe
+ * chunked prefill; it is the serving form of the same causal forward.
+ */
+plx_status plx_prefill_fwd_chunk(const void *q, const void *k, const void *v, const void *r,
+                                 void *out, float *lse, int B, int Hq, int Hkv, int Lq, int Lk,
+                                 int d, void *stream);
+
+/*
  * Causal prefill in fp32 (CUDA cores, fp32 arithmetic throughout). Same
  * arguments and layouts as plx_prefill_fwd with float tensors; d in {64, 128}.
  * This is the exact-arithmetic path used to check parity at 1e-5 relative error.

@@ -29,6 +29,7 @@ _vp, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_lon
 SIGNATURES = {
     "plx_prefill_fwd": (_i, [_vp] * 6 + [_i] * 5 + [_vp]),
     "plx_prefill_fwd_f32": (_i, [_vp] * 6 + [_i] * 5 + [_vp]),
+    "plx_prefill_fwd_chunk": (_i, [_vp] * 6 + [_i] * 6 + [_vp]),
     "plx_decode_fwd": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
     "plx_decode_fwd_ex": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
     "plx_decode_fwd_noalloc": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
@@ -127,6 +128,36 @@ def _prefill(fn, dtype, q, k, v, r, out, lse, stream):
 def plx_prefill_fwd(q, k, v, r, out=None, lse=None, stream=None):
     """Causal Parallax prefill, bf16 (see include/plx.h). Returns (out, lse)."""
     return _prefill(lib().plx_prefill_fwd, torch.bfloat16, q, k, v, r, out, lse, stream)
+
+
+def plx_prefill_fwd_chunk(q, k, v, r, out=None, lse=None, stream=None):
+    """Chunked causal prefill (see include/plx.h): q, r [B, Hq, Lq, d] are the
+    last Lq positions of k, v [B, Hkv, Lk, d]. Returns (out, lse)."""
+    _need(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("r", r)):
+        _need(t, name, torch.bfloat16, 4, dev)
+    B, Hq, Lq, d = q.shape
+    Hkv, Lk = k.shape[1], k.shape[2]
+    if tuple(r.shape) != tuple(q.shape):
+        raise ValueError("r must have the shape of q")
+    if tuple(k.shape) != (B, Hkv, Lk, d) or tuple(v.shape) != (B, Hkv, Lk, d):
+        raise ValueError("k and v must be [B, Hkv, Lk, d] matching q")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4, dev)
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have the shape of q")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3, dev)
+        if tuple(lse.shape) != (B, Hq, Lq):
+            raise ValueError("lse must be [B, Hq, Lq]")
+    with torch.cuda.device(dev):
+        st = lib().plx_prefill_fwd_chunk(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
+                                         out.data_ptr(), lse.data_ptr() if lse is not None else None,
+                                         B, Hq, Hkv, Lq, Lk, d, _stream(stream, dev))
+    _check(st)
+    return out, lse
 
 
 def plx_prefill_fwd_f32(q, k, v, r, out=None, lse=None, stream=None):

@@ -133,21 +133,29 @@ plx_status finish_launch(cudaError_t e, const char *fn) {
 
 extern "C" {
 
-plx_status plx_prefill_fwd(const void *q, const void *k, const void *v, const void *r, void *out,
-                           float *lse, int B, int Hq, int Hkv, int L, int d, void *stream) {
+plx_status plx_prefill_fwd_chunk(const void *q, const void *k, const void *v, const void *r,
+                                 void *out, float *lse, int B, int Hq, int Hkv, int Lq, int Lk,
+                                 int d, void *stream) {
   const char *fn = "plx_prefill_fwd";
   if (!q || !k || !v || !r || !out) return fail(PLX_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
-  plx_status s = check_common(fn, B, Hq, Hkv, L, d);
+  plx_status s = check_common(fn, B, Hq, Hkv, Lq, d);
   if (s) return s;
+  if (Lk < Lq) return fail(PLX_ERR_INVALID_ARG, "%s: Lk (%d) must be >= Lq (%d)", fn, Lk, Lq);
   if (d != 128) return fail(PLX_ERR_UNSUPPORTED, "%s: head dim %d (only 128)", fn, d);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(r) || !aligned16(out))
     return fail(PLX_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", fn);
-  if (static_cast<long long>(L + 127) / 128 * Hq * B > 0x7fffffffLL || static_cast<long long>(B) * Hq > 0x7fffffff)
+  if (static_cast<long long>(Lq + 127) / 128 * Hq * B > 0x7fffffffLL ||
+      static_cast<long long>(B) * Hq > 0x7fffffff)
     return fail(PLX_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
-  return finish_launch(plx::launch_prefill_tc(q, k, v, r, out, lse, B, Hq, Hkv, L,
+  return finish_launch(plx::launch_prefill_tc(q, k, v, r, out, lse, B, Hq, Hkv, Lq, Lk,
                                               plx::device_error_word(),
                                               static_cast<cudaStream_t>(stream)),
                        fn);
+}
+
+plx_status plx_prefill_fwd(const void *q, const void *k, const void *v, const void *r, void *out,
+                           float *lse, int B, int Hq, int Hkv, int L, int d, void *stream) {
+  return plx_prefill_fwd_chunk(q, k, v, r, out, lse, B, Hq, Hkv, L, L, d, stream);
 }
 
 plx_status plx_prefill_fwd_f32(const float *q, const float *k, const float *v, const float *r,

@@ -26,8 +26,9 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
                                unsigned *err, cudaStream_t stream);
 
 // Returns cudaErrorInvalidValue if a tensor map could not be encoded.
+// L queries, the last L positions of Lk >= L keys (Lk == L: plain prefill).
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *r, void *out,
-                              float *lse, int B, int Hq, int Hkv, int L, unsigned *err,
+                              float *lse, int B, int Hq, int Hkv, int L, int Lk, unsigned *err,
                               cudaStream_t stream);
 
 cudaError_t launch_decode(const void *q, const void *r, const void *kcache, const void *vcache,

@@ -11,6 +11,10 @@
 // finishes o = (O1 (1 + sigma / l) - O2) / l, i.e. o^SA - Sigma_KV rho
 // (section "Core mechanism").
 //
+// Chunked prefill: the L queries may be the last L positions of Lk >= L keys
+// (a new chunk against an existing cache); query row i then sees keys
+// 0 .. Lk - L + i. Plain prefill is Lk = L.
+//
 // Persistent: one CTA per SM walks a list of work items (128 query rows of
 // one (batch, head)), longest first, dealt to the CTAs in snake order so the
 // causal work evens out. TMEM, barriers and the pipelines stay up across
@@ -78,6 +82,7 @@ struct PrefillArgs {
   __nv_bfloat16 *out;
   float *lse;
   int Hq, Hkv, L, B, nqt, nitems;
+  int Lk, qoff;  // keys per head; absolute position of query row 0 (Lk - L)
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned *err;
 };
@@ -98,7 +103,7 @@ __device__ __forceinline__ bool item_of(const PrefillArgs &a, int k, Item &it) {
   const int rem = o % per_qt;
   const int h = rem % a.Hq, b = rem / a.Hq;
   it.q0 = qt * BM;
-  it.ntiles = (min(it.q0 + BM, a.L) + BN - 1) / BN;
+  it.ntiles = (min(a.qoff + it.q0 + BM, a.Lk) + BN - 1) / BN;
   it.zq = b * a.Hq + h;
   it.zk = b * a.Hkv + h / (a.Hq / a.Hkv);
   return true;
@@ -305,10 +310,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(cs, *reinterpret_cast<float(*)[32]>(&s[0]));
         tmem_ld32(cs + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
         tmem_wait_ld();
-        if (j * BN + BN - 1 > q0) {  // tile reaches the diagonal: causal mask
+        if (j * BN + BN - 1 > a.qoff + q0) {  // tile reaches the diagonal: causal mask
 #pragma unroll
           for (int e = 0; e < BN; ++e)
-            if (j * BN + e > grow) s[e] = -INFINITY;
+            if (j * BN + e > a.qoff + grow) s[e] = -INFINITY;
         }
         // Row max: 8 independent chains of 3-input max, then a tree.
         float mx8[8];
@@ -461,7 +466,7 @@ bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, int L, int h
 }  // namespace
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *r, void *out,
-                              float *lse, int B, int Hq, int Hkv, int L, unsigned *err,
+                              float *lse, int B, int Hq, int Hkv, int L, int Lk, unsigned *err,
                               cudaStream_t stream) {
   static thread_local int configured_device = -1;
   int dev = 0;
@@ -476,7 +481,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
   if (enc == nullptr) return cudaErrorInvalidValue;
   CUtensorMap mq, mr, mk, mv;
   if (!make_map(enc, &mq, q, L, B * Hq, BM) || !make_map(enc, &mr, r, L, B * Hq, BM) ||
-      !make_map(enc, &mk, k, L, B * Hkv, BN) || !make_map(enc, &mv, v, L, B * Hkv, BN))
+      !make_map(enc, &mk, k, Lk, B * Hkv, BN) || !make_map(enc, &mv, v, Lk, B * Hkv, BN))
     return cudaErrorInvalidValue;
   PrefillArgs a;
   a.out = static_cast<__nv_bfloat16 *>(out);
@@ -484,6 +489,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.L = L;
+  a.Lk = Lk;
+  a.qoff = Lk - L;
   a.B = B;
   a.nqt = (L + BM - 1) / BM;
   a.nitems = a.nqt * Hq * B;

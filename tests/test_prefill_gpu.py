@@ -106,3 +106,43 @@ def test_bf16_rejects_bad_head_dim():
     q = torch.zeros(1, 2, 16, 64, dtype=torch.bfloat16, device=dev)
     with pytest.raises(PlxError, match="head dim"):
         plx_prefill_fwd(q, q[:, :1].contiguous(), q[:, :1].contiguous(), q)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk", [
+    (1, 2, 1, 1, 300),      # a single new token over a cache
+    (2, 4, 2, 77, 333),     # offset not a multiple of the tile sizes
+    (1, 2, 2, 200, 200),    # Lq == Lk: plain prefill
+    (1, 4, 2, 129, 1000),   # a chunk just over one query tile
+])
+def test_bf16_chunked_prefill_matches_oracle(B, Hq, Hkv, Lq, Lk):
+    from parametrized_local_linear_gb300 import plx_prefill_fwd_chunk
+    dev = device()
+    q, k, v, r = inputs.prefill_inputs(B, Hq, Hkv, Lk, 128, torch.bfloat16, 0.05, Lq + Lk)
+    qc, rc = q[:, :, -Lq:].contiguous(), r[:, :, -Lq:].contiguous()
+    out = torch.full(qc.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full(qc.shape[:3], float("nan"), device=dev)
+    plx_prefill_fwd_chunk(qc.to(dev), k.to(dev), v.to(dev), rc.to(dev), out, lse)
+    plx_check_device_error()
+    ref, ref_lse = oracle.prefill(qc, k, v, rc)
+    assert_bf16_close(out.double().cpu().numpy(), ref, "chunk")
+    np.testing.assert_allclose(lse.double().cpu().numpy(), ref_lse, rtol=0, atol=2e-3)
+
+
+def test_bf16_chunk_equals_tail_of_full_prefill_on_gpu():
+    from parametrized_local_linear_gb300 import plx_prefill_fwd_chunk
+    dev = device()
+    q, k, v, r = (t.to(dev) for t in inputs.prefill_inputs(2, 4, 2, 700, 128, torch.bfloat16, 0.05, 8))
+    full, _ = plx_prefill_fwd(q, k, v, r)
+    part, _ = plx_prefill_fwd_chunk(q[:, :, 500:].contiguous(), k, v, r[:, :, 500:].contiguous())
+    plx_check_device_error()
+    # Same keys, same tiles, same arithmetic per row: bit-identical.
+    assert torch.equal(part, full[:, :, 500:])
+
+
+def test_chunk_rejects_lq_above_lk():
+    from parametrized_local_linear_gb300 import plx_prefill_fwd_chunk
+    dev = device()
+    q = torch.zeros(1, 2, 64, 128, dtype=torch.bfloat16, device=dev)
+    k = torch.zeros(1, 1, 32, 128, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(PlxError, match="Lk"):
+        plx_prefill_fwd_chunk(q, k, k, q)
