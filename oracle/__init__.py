@@ -18,6 +18,11 @@ with gcc, loads it with ctypes and walks the (batch, head, row) index space:
 * ``decode``: one query per (sequence, head) sees all ``seqlens[b]`` cached
   keys; the cache is packed ``[sum(seqlens), Hkv, d]``.
 
+With ``with_cor=True`` both also return the correction-to-output ratio
+|Sigma rho| / |o| per query (0 where |o| = 0), the COR that the same page
+reports in its experimental results; the norms are Euclidean (a reading: the
+pages give no formula).
+
 Inputs may be numpy arrays or CPU torch tensors of any float dtype; every
 slice is upcast to float64 before the C code sees it, so the oracle works on
 exactly the (bf16- or fp32-rounded) values a device kernel receives.
@@ -63,10 +68,10 @@ def _load():
             lib = ctypes.CDLL(build())
             dp = ctypes.POINTER(ctypes.c_double)
             lib.plx_oracle_query.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_double, dp, dp,
-                                             dp, ctypes.c_long, dp, ctypes.c_long, dp, dp, dp]
+                                             dp, ctypes.c_long, dp, ctypes.c_long, dp, dp, dp, dp]
             lib.plx_oracle_query.restype = ctypes.c_int
             lib.plx_oracle_rows.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int,
-                                            ctypes.c_double, dp, dp, dp, dp, dp, dp]
+                                            ctypes.c_double, dp, dp, dp, dp, dp, dp, dp]
             lib.plx_oracle_rows.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -88,49 +93,57 @@ def default_threads() -> int:
     return max(1, len(os.sched_getaffinity(0)))
 
 
-def query(q, rho, K, V, tau=None, with_sigma=False):
+def query(q, rho, K, V, tau=None, with_sigma=False, with_cor=False):
     """One query vector against all rows of K and V (n x d).
 
-    Returns (o, lse) or (o, lse, Sigma) with Sigma[a, c] = value dim a, key dim c.
+    Returns (o, lse), then Sigma (Sigma[a, c] = value dim a, key dim c) if
+    ``with_sigma``, then cor = |Sigma rho| / |o| if ``with_cor``.
     """
     lib = _load()
     q = _f64(q); rho = _f64(rho); K = _f64(K); V = _f64(V)
     n, d = K.shape if K.ndim == 2 else (0, q.shape[0])
     tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
-    out = np.empty(d); lse = np.empty(1)
+    out = np.empty(d); lse = np.empty(1); cor = np.empty(1)
     sig = np.empty((d, d)) if with_sigma else None
     if n == 0:
         K = np.zeros((1, d)); V = np.zeros((1, d))
     rc = lib.plx_oracle_query(n, d, tau, _ptr(q), _ptr(rho), _ptr(K), d, _ptr(V), d,
-                              _ptr(out), _ptr(lse), _ptr(sig) if with_sigma else None)
+                              _ptr(out), _ptr(lse), _ptr(sig) if with_sigma else None,
+                              _ptr(cor) if with_cor else None)
     if rc:
         raise MemoryError("oracle allocation failed")
-    return (out, float(lse[0]), sig) if with_sigma else (out, float(lse[0]))
+    res = (out, float(lse[0]))
+    if with_sigma:
+        res += (sig,)
+    if with_cor:
+        res += (float(cor[0]),)
+    return res
 
 
 def _rows(nkeys, Q, R, K, V, tau):
     lib = _load()
     nkeys = np.ascontiguousarray(nkeys, dtype=np.int32)
     n, d = Q.shape
-    out = np.empty((n, d)); lse = np.empty(n)
+    out = np.empty((n, d)); lse = np.empty(n); cor = np.empty(n)
     if K.shape[0] == 0:
         K = np.zeros((1, d)); V = np.zeros((1, d))
     rc = lib.plx_oracle_rows(n, nkeys.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), d, tau,
-                             _ptr(Q), _ptr(R), _ptr(K), _ptr(V), _ptr(out), _ptr(lse))
+                             _ptr(Q), _ptr(R), _ptr(K), _ptr(V), _ptr(out), _ptr(lse), _ptr(cor))
     if rc:
         raise MemoryError("oracle allocation failed")
-    return out, lse
+    return out, lse, cor
 
 
-def prefill(q, k, v, r, rows=None, threads=None):
+def prefill(q, k, v, r, rows=None, threads=None, with_cor=False):
     """Causal Parallax prefill.
 
     q, r: [B, Hq, L, d]; k, v: [B, Hkv, Lk, d] with Lk >= L. The L queries are
     the last L of the Lk positions, so query i sees keys 0 .. Lk - L + i
     (Lk == L: ordinary causal prefill; Lk > L: a chunk appended to an existing
     cache). ``rows`` is None (every row) or an iterable of (b, h, i). Returns
-    (out, lse): with rows=None, out is [B, Hq, L, d] and lse [B, Hq, L];
-    otherwise out is [n, d], lse [n] in the order of ``rows``.
+    (out, lse), or (out, lse, cor) with ``with_cor``: with rows=None, out is
+    [B, Hq, L, d] and lse, cor [B, Hq, L]; otherwise out is [n, d], lse and
+    cor [n] in the order of ``rows``.
     """
     B, Hq, L, d = q.shape
     Hkv = k.shape[1]
@@ -148,7 +161,7 @@ def prefill(q, k, v, r, rows=None, threads=None):
     groups = {}
     for n, (b, h, i) in enumerate(rows):
         groups.setdefault((b, h), []).append((n, i))
-    out = np.empty((len(rows), d)); lse = np.empty(len(rows))
+    out = np.empty((len(rows), d)); lse = np.empty(len(rows)); cor = np.empty(len(rows))
 
     def work(key):
         b, h = key
@@ -156,22 +169,23 @@ def prefill(q, k, v, r, rows=None, threads=None):
         idx = np.array([i for _, i in items])
         Kb = _f64(k[b, h // G]); Vb = _f64(v[b, h // G])
         Qb = _f64(q[b, h])[idx]; Rb = _f64(r[b, h])[idx]
-        o, l = _rows(offset + idx + 1, Qb, Rb, Kb, Vb, tau)
-        for (n, _), on, ln in zip(items, o, l):
-            out[n] = on; lse[n] = ln
+        o, l, c = _rows(offset + idx + 1, Qb, Rb, Kb, Vb, tau)
+        for (n, _), on, ln, cn in zip(items, o, l, c):
+            out[n] = on; lse[n] = ln; cor[n] = cn
 
     _parallel(work, list(groups), threads)
     if full:
-        return out.reshape(B, Hq, L, d), lse.reshape(B, Hq, L)
-    return out, lse
+        out, lse, cor = out.reshape(B, Hq, L, d), lse.reshape(B, Hq, L), cor.reshape(B, Hq, L)
+    return (out, lse, cor) if with_cor else (out, lse)
 
 
-def decode(q, r, kcache, vcache, seqlens, pairs=None, threads=None):
+def decode(q, r, kcache, vcache, seqlens, pairs=None, threads=None, with_cor=False):
     """Parallax decode: one query per (sequence b, head h) over its whole cache.
 
     q, r: [B, Hq, d]; kcache, vcache: packed [sum(seqlens), Hkv, d], sequence b
     at token offset sum(seqlens[:b]). ``pairs`` is None (all) or an iterable of
-    (b, h). Returns (out, lse) shaped [B, Hq, d] / [B, Hq] or [n, d] / [n].
+    (b, h). Returns (out, lse) shaped [B, Hq, d] / [B, Hq] or [n, d] / [n],
+    and cor shaped like lse after them with ``with_cor``.
     """
     B, Hq, d = q.shape
     Hkv = kcache.shape[1]
@@ -181,19 +195,19 @@ def decode(q, r, kcache, vcache, seqlens, pairs=None, threads=None):
     offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
     full = pairs is None
     pairs = [(b, h) for b in range(B) for h in range(Hq)] if full else [tuple(p) for p in pairs]
-    out = np.empty((len(pairs), d)); lse = np.empty(len(pairs))
+    out = np.empty((len(pairs), d)); lse = np.empty(len(pairs)); cor = np.empty(len(pairs))
 
     def work(n):
         b, h = pairs[n]
         lo, hi = int(offs[b]), int(offs[b + 1])
         Kb = _f64(kcache[lo:hi, h // G]); Vb = _f64(vcache[lo:hi, h // G])
-        o, l = _rows(np.array([hi - lo]), _f64(q[b, h])[None], _f64(r[b, h])[None], Kb, Vb, tau)
-        out[n] = o[0]; lse[n] = l[0]
+        o, l, c = _rows(np.array([hi - lo]), _f64(q[b, h])[None], _f64(r[b, h])[None], Kb, Vb, tau)
+        out[n] = o[0]; lse[n] = l[0]; cor[n] = c[0]
 
     _parallel(work, list(range(len(pairs))), threads)
     if full:
-        return out.reshape(B, Hq, d), lse.reshape(B, Hq)
-    return out, lse
+        out, lse, cor = out.reshape(B, Hq, d), lse.reshape(B, Hq), cor.reshape(B, Hq)
+    return (out, lse, cor) if with_cor else (out, lse)
 
 
 def _parallel(fn, items, threads):

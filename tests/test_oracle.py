@@ -256,3 +256,77 @@ def test_chunked_prefill_is_the_tail_of_the_full_prefill():
         out, lse = oracle.prefill(q[:, :, -lq:].contiguous(), k, v, r[:, :, -lq:].contiguous())
         np.testing.assert_array_equal(out, full[:, :, -lq:])
         np.testing.assert_array_equal(lse, flse[:, :, -lq:])
+
+
+# --- COR: the correction-to-output ratio |Sigma rho| / |o| per query ---------
+# (the page's experimental results report COR per layer; the pages give no
+# formula, and the ratio of Euclidean norms per query is the reading pinned.)
+
+@pytest.mark.parametrize("n,d", [(2, 3), (17, 8), (150, 16)])
+def test_cor_against_library_covariance(n, d):
+    """COR from numpy's weighted covariance and scipy's softmax, with o built
+    from those too: catches a ratio taken against o^SA instead of o, a squared
+    norm, or the wrong branch in the numerator."""
+    rng = np.random.default_rng(n * 31 + d)
+    q = rng.normal(size=d); rho = rng.normal(size=d) * 0.3
+    K = rng.normal(size=(n, d)); V = rng.normal(size=(n, d))
+    _, _, cor = oracle.query(q, rho, K, V, with_cor=True)
+    w = scipy.special.softmax(K @ q / math.sqrt(d))
+    sig = np.cov(np.vstack([V.T, K.T]), aweights=w, bias=True)[:d, d:]
+    corr = sig @ rho
+    ref = np.linalg.norm(corr) / np.linalg.norm(w @ V - corr)
+    assert abs(cor - ref) <= 1e-12 * max(1.0, ref)
+
+
+def test_cor_two_keys_closed_form():
+    """Two keys: |Sigma rho| = w0 w1 |(k1 - k0).rho| |v1 - v0|."""
+    rng = np.random.default_rng(12)
+    d = 6
+    q = rng.normal(size=d); rho = rng.normal(size=d)
+    K = rng.normal(size=(2, d)); V = rng.normal(size=(2, d))
+    o, _, cor = oracle.query(q, rho, K, V, with_cor=True)
+    s = K @ q / math.sqrt(d)
+    w0 = 1.0 / (1.0 + math.exp(s[1] - s[0])); w1 = 1.0 - w0
+    num = w0 * w1 * abs((K[1] - K[0]) @ rho) * math.sqrt(((V[1] - V[0]) ** 2).sum())
+    assert abs(cor - num / math.sqrt((o ** 2).sum())) < 1e-12
+
+
+def test_cor_zero_cases():
+    """One key (Sigma = 0), rho = 0, and an empty key set all give 0."""
+    rng = np.random.default_rng(13)
+    d = 5
+    q = rng.normal(size=d); rho = rng.normal(size=d)
+    K = rng.normal(size=(7, d)); V = rng.normal(size=(7, d))
+    assert oracle.query(q, rho, K[:1], V[:1], with_cor=True)[2] == 0.0
+    assert oracle.query(q, np.zeros(d), K, V, with_cor=True)[2] == 0.0
+    assert oracle.query(q, rho, K[:0], V[:0], with_cor=True)[2] == 0.0
+
+
+def test_cor_is_invariant_to_value_scale():
+    """Scaling every v by c > 0 scales both Sigma rho and o by c."""
+    rng = np.random.default_rng(14)
+    d = 8
+    q = rng.normal(size=d); rho = rng.normal(size=d)
+    K = rng.normal(size=(30, d)); V = rng.normal(size=(30, d))
+    c1 = oracle.query(q, rho, K, V, with_cor=True)[2]
+    c2 = oracle.query(q, rho, K, 3.5 * V, with_cor=True)[2]
+    assert c1 > 0 and abs(c1 - c2) < 1e-12 * c1
+
+
+def test_cor_prefill_and_decode_agree_with_query():
+    """The batched walks return the per-query ratio (GQA mapping, causal
+    window and packing as for the outputs)."""
+    g = torch.Generator().manual_seed(15)
+    B, Hq, Hkv, L, d = 2, 4, 2, 9, 8
+    q, k, v, r = (torch.randn(B, h, L, d, generator=g, dtype=torch.float64) for h in (Hq, Hkv, Hkv, Hq))
+    _, _, cor = oracle.prefill(q, k, v, r, with_cor=True)
+    for b, h, i in [(0, 0, 0), (0, 3, 4), (1, 2, 8), (1, 1, 1)]:
+        ref = oracle.query(q[b, h, i].numpy(), r[b, h, i].numpy(), k[b, h // 2, :i + 1].numpy(),
+                           v[b, h // 2, :i + 1].numpy(), with_cor=True)[2]
+        assert abs(cor[b, h, i] - ref) < 1e-14
+    seqlens = torch.tensor([9, 0])
+    kc = torch.cat([k[0].transpose(0, 1), k[1, :, :0].transpose(0, 1)])
+    vc = torch.cat([v[0].transpose(0, 1), v[1, :, :0].transpose(0, 1)])
+    _, _, dcor = oracle.decode(q[:, :, -1], r[:, :, -1], kc, vc, seqlens, with_cor=True)
+    np.testing.assert_allclose(dcor[0], cor[0, :, -1], rtol=0, atol=1e-14)
+    assert np.all(dcor[1] == 0.0)
