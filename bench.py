@@ -355,54 +355,52 @@ def main():
     extra = {}
     if not args.no_extra:
         del hq, hd
+        from parametrized_local_linear_gb300 import (plx_decode_fwd_cor, plx_prefill_fwd_chunk,
+                                                     plx_prefill_fwd_cor)
+        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+
+        def launch_s(fn, n):
+            """Mean seconds per call of fn() over n back-to-back calls after 3
+            untimed ones (CUDA events on the launching stream)."""
+            for _ in range(3):
+                fn()
+            a.record(stream)
+            for _ in range(n):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / n * 1e-3
+
+        def tflops(name, flops, t):
+            extra[name] = {"value": flops / t / 1e12, "unit": "TFLOP/s", "ms": t * 1e3,
+                           "frac_of_peak": flops / t / 1e12 / tc_peak}
+
         w3 = inputs.PREFILL_1P7B
         q3, k3, v3, r3 = inputs.prefill_inputs_for(w3, device=dev)
         o3 = torch.empty_like(q3)
-        for _ in range(3):
-            plx_prefill_fwd(q3, k3, v3, r3, o3)
-        a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
-        n3 = 5
-        a.record(stream)
-        for _ in range(n3):
-            plx_prefill_fwd(q3, k3, v3, r3, o3)
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        t3 = a.elapsed_time(b) / n3 * 1e-3
-        extra[w3.name] = {"value": w3.flops / t3 / 1e12, "unit": "TFLOP/s", "ms": t3 * 1e3,
-                          "frac_of_peak": w3.flops / t3 / 1e12 / tc_peak}
+        tflops(w3.name, w3.flops, launch_s(lambda: plx_prefill_fwd(q3, k3, v3, r3, o3), 5))
         # Chunked prefill: the last 2048 positions of a 16384-token sequence
         # (a new chunk against an existing cache), 1.7B-shaped heads.
-        from parametrized_local_linear_gb300 import plx_prefill_fwd_chunk
-        lq = 2048
+        lq, lk = 2048, w3.L
         qc, rc = q3[:, :, -lq:].contiguous(), r3[:, :, -lq:].contiguous()
         oc = torch.empty_like(qc)
-        for _ in range(3):
-            plx_prefill_fwd_chunk(qc, k3, v3, rc, oc)
-        a.record(stream)
-        for _ in range(n3):
-            plx_prefill_fwd_chunk(qc, k3, v3, rc, oc)
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        tc = a.elapsed_time(b) / n3 * 1e-3
-        lk = w3.L
         cflops = 8 * w3.d * w3.B * w3.Hq * (lq * (lk - lq) + lq * (lq + 1) // 2)
-        extra["prefill_chunk_Lq2048_Lk16384_B1_Hq16_Hkv8_d128"] = {
-            "value": cflops / tc / 1e12, "unit": "TFLOP/s", "ms": tc * 1e3,
-            "frac_of_peak": cflops / tc / 1e12 / tc_peak}
+        tflops("prefill_chunk_Lq2048_Lk16384_B1_Hq16_Hkv8_d128", cflops,
+               launch_s(lambda: plx_prefill_fwd_chunk(qc, k3, v3, rc, oc), 5))
         del q3, k3, v3, r3, o3, qc, rc, oc
+        # The correction-to-output ratio as a side output of the same calls.
+        cor = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        tflops(wp.name + "_with_cor", wp.flops,
+               launch_s(lambda: plx_prefill_fwd_cor(q, k, v, r, out, None, cor), 10))
+        dcor = torch.empty(dq.shape[:2], dtype=torch.float32, device=dev)
+        td = launch_s(lambda: plx_decode_fwd_cor(dq, dr, kc, vc, sl, dout, dcor), 10)
+        extra[wd.name + "_with_cor"] = {"value": dbytes / td / 1e9, "unit": "GB/s", "ms": td * 1e3,
+                                        "frac_of_peak": dbytes / td / 1e9 / hbm_peak}
         w5 = inputs.DECODE_RAGGED
         d5 = inputs.decode_inputs_for(w5, device=dev)
         sl5 = d5[4].to(dev)
         o5 = torch.empty_like(d5[0])
-        for _ in range(3):
-            plx_decode_fwd(d5[0], d5[1], d5[2], d5[3], sl5, o5)
-        n5 = 10
-        a.record(stream)
-        for _ in range(n5):
-            plx_decode_fwd(d5[0], d5[1], d5[2], d5[3], sl5, o5)
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        t5 = a.elapsed_time(b) / n5 * 1e-3
+        t5 = launch_s(lambda: plx_decode_fwd(d5[0], d5[1], d5[2], d5[3], sl5, o5), 10)
         by5 = w5.bytes_moved()
         extra[w5.name] = {"value": by5 / t5 / 1e9, "unit": "GB/s", "ms": t5 * 1e3,
                           "bytes": by5, "seqlens": w5.seqlens().tolist(),

@@ -83,6 +83,23 @@ plx_status plx_prefill_fwd_chunk(const void *q, const void *k, const void *v, co
                                  int d, void *stream);
 
 /*
+ * Chunked prefill with a per-row side output: the correction-to-output ratio
+ * COR, which the page "Parallax: parametrized local linear attention for
+ * language modeling" reports per layer in its experimental results (optimizer
+ * dependence) without giving a formula. Reading used here, per query row:
+ *   cor = |Sigma_KV rho| / |o|   (Euclidean norms over the d values of the
+ *                                 fp32 correction and output before the bf16
+ *                                 rounding of o; 0 when |o| = 0)
+ * Arguments, layouts and results as plx_prefill_fwd_chunk, plus
+ *   cor : fp32 [B, Hq, Lq], must not be NULL.
+ * A per-layer COR is the mean (or any other statistic) of cor over rows,
+ * taken by the caller.
+ */
+plx_status plx_prefill_fwd_cor(const void *q, const void *k, const void *v, const void *r,
+                               void *out, float *lse, float *cor, int B, int Hq, int Hkv, int Lq,
+                               int Lk, int d, void *stream);
+
+/*
  * Causal prefill in fp32 (CUDA cores, fp32 arithmetic throughout). Same
  * arguments and layouts as plx_prefill_fwd with float tensors; d in {64, 128}.
  * This is the exact-arithmetic path used to check parity at 1e-5 relative error.
@@ -121,6 +138,18 @@ plx_status plx_decode_fwd(const void *q, const void *r, const void *kcache, cons
 plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, const void *vcache,
                              const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
                              int nsplit, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Decode with the per-(sequence, head) correction-to-output ratio (see
+ * plx_prefill_fwd_cor for the reading): arguments, layouts, allocation and
+ * results as plx_decode_fwd, plus
+ *   cor : fp32 [B, Hq], must not be NULL; 0 for sequences of length 0.
+ * The ratio is formed after the split records are combined, from the
+ * combined fp32 correction and output.
+ */
+plx_status plx_decode_fwd_cor(const void *q, const void *r, const void *kcache, const void *vcache,
+                              const int *seqlens, void *out, float *cor, int B, int Hq, int Hkv,
+                              int d, void *stream);
 
 /*
  * plx_decode_fwd for callers that cannot allocate device memory during the

@@ -30,9 +30,11 @@ SIGNATURES = {
     "plx_prefill_fwd": (_i, [_vp] * 6 + [_i] * 5 + [_vp]),
     "plx_prefill_fwd_f32": (_i, [_vp] * 6 + [_i] * 5 + [_vp]),
     "plx_prefill_fwd_chunk": (_i, [_vp] * 6 + [_i] * 6 + [_vp]),
+    "plx_prefill_fwd_cor": (_i, [_vp] * 7 + [_i] * 6 + [_vp]),
     "plx_decode_fwd": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
     "plx_decode_fwd_ex": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
     "plx_decode_fwd_noalloc": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
+    "plx_decode_fwd_cor": (_i, [_vp] * 7 + [_i] * 4 + [_vp]),
     "plx_decode_workspace_bytes": (_sz, [_i] * 4),
     "plx_decode_default_nsplit": (_i, [_i] * 2),
     "plx_check_device_error": (_i, [_vp]),
@@ -133,6 +135,20 @@ def plx_prefill_fwd(q, k, v, r, out=None, lse=None, stream=None):
 def plx_prefill_fwd_chunk(q, k, v, r, out=None, lse=None, stream=None):
     """Chunked causal prefill (see include/plx.h): q, r [B, Hq, Lq, d] are the
     last Lq positions of k, v [B, Hkv, Lk, d]. Returns (out, lse)."""
+    out, lse, _ = _prefill_chunk(q, k, v, r, out, lse, None, stream)
+    return out, lse
+
+
+def plx_prefill_fwd_cor(q, k, v, r, out=None, lse=None, cor=None, stream=None):
+    """Chunked causal prefill that also writes the correction-to-output ratio
+    |Sigma rho| / |o| per row (see include/plx.h). ``cor`` is fp32
+    [B, Hq, Lq] (allocated if None). Returns (out, lse, cor)."""
+    if cor is None:
+        cor = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    return _prefill_chunk(q, k, v, r, out, lse, cor, stream)
+
+
+def _prefill_chunk(q, k, v, r, out, lse, cor, stream):
     _need(q, "q", torch.bfloat16, 4)
     dev = q.device
     for name, t in (("k", k), ("v", v), ("r", r)):
@@ -148,16 +164,23 @@ def plx_prefill_fwd_chunk(q, k, v, r, out=None, lse=None, stream=None):
     _need(out, "out", torch.bfloat16, 4, dev)
     if tuple(out.shape) != tuple(q.shape):
         raise ValueError("out must have the shape of q")
-    if lse is not None:
-        _need(lse, "lse", torch.float32, 3, dev)
-        if tuple(lse.shape) != (B, Hq, Lq):
-            raise ValueError("lse must be [B, Hq, Lq]")
+    for name, t in (("lse", lse), ("cor", cor)):
+        if t is not None:
+            _need(t, name, torch.float32, 3, dev)
+            if tuple(t.shape) != (B, Hq, Lq):
+                raise ValueError(f"{name} must be [B, Hq, Lq]")
+    lse_ptr = lse.data_ptr() if lse is not None else None
     with torch.cuda.device(dev):
-        st = lib().plx_prefill_fwd_chunk(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
-                                         out.data_ptr(), lse.data_ptr() if lse is not None else None,
-                                         B, Hq, Hkv, Lq, Lk, d, _stream(stream, dev))
+        if cor is None:
+            st = lib().plx_prefill_fwd_chunk(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
+                                             out.data_ptr(), lse_ptr, B, Hq, Hkv, Lq, Lk, d,
+                                             _stream(stream, dev))
+        else:
+            st = lib().plx_prefill_fwd_cor(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
+                                           out.data_ptr(), lse_ptr, cor.data_ptr(), B, Hq, Hkv, Lq,
+                                           Lk, d, _stream(stream, dev))
     _check(st)
-    return out, lse
+    return out, lse, cor
 
 
 def plx_prefill_fwd_f32(q, k, v, r, out=None, lse=None, stream=None):
@@ -223,6 +246,37 @@ def plx_decode_fwd_noalloc(q, r, kcache, vcache, seqlens, out, stream=None):
                                           B, Hq, kcache.shape[1], d, _stream(stream, dev))
     _check(st)
     return out
+
+
+def plx_decode_fwd_cor(q, r, kcache, vcache, seqlens, out=None, cor=None, stream=None):
+    """Decode that also writes the correction-to-output ratio |Sigma rho| / |o|
+    per (sequence, head) (see include/plx.h). ``cor`` is fp32 [B, Hq]
+    (allocated if None). Returns (out, cor)."""
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    for name, t in (("r", r), ("kcache", kcache), ("vcache", vcache)):
+        _need(t, name, torch.bfloat16, 3, dev)
+    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    B, Hq, d = q.shape
+    if tuple(r.shape) != tuple(q.shape) or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("r must match q and vcache must match kcache")
+    if kcache.shape[2] != d or seqlens.shape[0] != B:
+        raise ValueError("kcache must be [T, Hkv, d] and seqlens [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    if cor is None:
+        cor = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    _need(cor, "cor", torch.float32, 2, dev)
+    if tuple(out.shape) != tuple(q.shape) or tuple(cor.shape) != (B, Hq):
+        raise ValueError("out must have the shape of q and cor be [B, Hq]")
+    with torch.cuda.device(dev):
+        st = lib().plx_decode_fwd_cor(q.data_ptr(), r.data_ptr(), kcache.data_ptr(),
+                                      vcache.data_ptr(), seqlens.data_ptr(), out.data_ptr(),
+                                      cor.data_ptr(), B, Hq, kcache.shape[1], d,
+                                      _stream(stream, dev))
+    _check(st)
+    return out, cor
 
 
 def plx_decode_workspace_bytes(B, Hq, d, nsplit) -> int:

@@ -133,10 +133,11 @@ plx_status finish_launch(cudaError_t e, const char *fn) {
 
 extern "C" {
 
-plx_status plx_prefill_fwd_chunk(const void *q, const void *k, const void *v, const void *r,
-                                 void *out, float *lse, int B, int Hq, int Hkv, int Lq, int Lk,
-                                 int d, void *stream) {
-  const char *fn = "plx_prefill_fwd";
+namespace {
+
+plx_status prefill_bf16(const char *fn, const void *q, const void *k, const void *v, const void *r,
+                        void *out, float *lse, float *cor, int B, int Hq, int Hkv, int Lq, int Lk,
+                        int d, void *stream) {
   if (!q || !k || !v || !r || !out) return fail(PLX_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
   plx_status s = check_common(fn, B, Hq, Hkv, Lq, d);
   if (s) return s;
@@ -147,10 +148,27 @@ plx_status plx_prefill_fwd_chunk(const void *q, const void *k, const void *v, co
   if (static_cast<long long>(Lq + 127) / 128 * Hq * B > 0x7fffffffLL ||
       static_cast<long long>(B) * Hq > 0x7fffffff)
     return fail(PLX_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
-  return finish_launch(plx::launch_prefill_tc(q, k, v, r, out, lse, B, Hq, Hkv, Lq, Lk,
+  return finish_launch(plx::launch_prefill_tc(q, k, v, r, out, lse, cor, B, Hq, Hkv, Lq, Lk,
                                               plx::device_error_word(),
                                               static_cast<cudaStream_t>(stream)),
                        fn);
+}
+
+}  // namespace
+
+plx_status plx_prefill_fwd_chunk(const void *q, const void *k, const void *v, const void *r,
+                                 void *out, float *lse, int B, int Hq, int Hkv, int Lq, int Lk,
+                                 int d, void *stream) {
+  return prefill_bf16("plx_prefill_fwd", q, k, v, r, out, lse, nullptr, B, Hq, Hkv, Lq, Lk, d,
+                      stream);
+}
+
+plx_status plx_prefill_fwd_cor(const void *q, const void *k, const void *v, const void *r,
+                               void *out, float *lse, float *cor, int B, int Hq, int Hkv, int Lq,
+                               int Lk, int d, void *stream) {
+  if (!cor) return fail(PLX_ERR_INVALID_ARG, "plx_prefill_fwd_cor: null cor pointer");
+  return prefill_bf16("plx_prefill_fwd_cor", q, k, v, r, out, lse, cor, B, Hq, Hkv, Lq, Lk, d,
+                      stream);
 }
 
 plx_status plx_prefill_fwd(const void *q, const void *k, const void *v, const void *r, void *out,
@@ -194,10 +212,12 @@ int plx_decode_default_nsplit(int B, int Hkv) {
   return static_cast<int>(n);
 }
 
-plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, const void *vcache,
-                             const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
-                             int nsplit, void *workspace, size_t workspace_bytes, void *stream) {
-  const char *fn = "plx_decode_fwd";
+namespace {
+
+plx_status decode_bf16(const char *fn, const void *q, const void *r, const void *kcache,
+                       const void *vcache, const int *seqlens, void *out, float *cor, int B,
+                       int Hq, int Hkv, int d, int nsplit, void *workspace, size_t workspace_bytes,
+                       void *stream) {
   if (!q || !r || !kcache || !vcache || !seqlens || !out)
     return fail(PLX_ERR_INVALID_ARG, "%s: null pointer", fn);
   plx_status s = check_common(fn, B, Hq, Hkv, 1, d);
@@ -218,20 +238,37 @@ plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, c
       return fail(PLX_ERR_INVALID_ARG, "%s: workspace of %zu bytes, need %zu", fn, workspace_bytes,
                   need);
     if (!aligned16(workspace)) return fail(PLX_ERR_INVALID_ARG, "%s: workspace not 16-byte aligned", fn);
-    return finish_launch(plx::launch_decode(q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, nsplit,
-                                            static_cast<float *>(workspace),
+    return finish_launch(plx::launch_decode(q, r, kcache, vcache, seqlens, out, cor, B, Hq, Hkv,
+                                            nsplit, static_cast<float *>(workspace),
                                             plx::device_error_word(), st),
                          fn);
   }
   void *ws = nullptr;
   cudaError_t e = cudaMallocAsync(&ws, need, st);
   if (e != cudaSuccess) return cuda_fail(e, "plx_decode_fwd: workspace allocation");
-  e = plx::launch_decode(q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, nsplit,
+  e = plx::launch_decode(q, r, kcache, vcache, seqlens, out, cor, B, Hq, Hkv, nsplit,
                          static_cast<float *>(ws), plx::device_error_word(), st);
   cudaError_t e2 = cudaFreeAsync(ws, st);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   if (e2 != cudaSuccess) return cuda_fail(e2, "plx_decode_fwd: workspace release");
   return PLX_OK;
+}
+
+}  // namespace
+
+plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, const void *vcache,
+                             const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
+                             int nsplit, void *workspace, size_t workspace_bytes, void *stream) {
+  return decode_bf16("plx_decode_fwd", q, r, kcache, vcache, seqlens, out, nullptr, B, Hq, Hkv, d,
+                     nsplit, workspace, workspace_bytes, stream);
+}
+
+plx_status plx_decode_fwd_cor(const void *q, const void *r, const void *kcache, const void *vcache,
+                              const int *seqlens, void *out, float *cor, int B, int Hq, int Hkv,
+                              int d, void *stream) {
+  if (!cor) return fail(PLX_ERR_INVALID_ARG, "plx_decode_fwd_cor: null cor pointer");
+  return decode_bf16("plx_decode_fwd_cor", q, r, kcache, vcache, seqlens, out, cor, B, Hq, Hkv, d,
+                     0, nullptr, 0, stream);
 }
 
 plx_status plx_decode_fwd(const void *q, const void *r, const void *kcache, const void *vcache,

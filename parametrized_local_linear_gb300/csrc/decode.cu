@@ -296,12 +296,12 @@ __global__ void __launch_bounds__(THREADS)
 // One block of D threads per (sequence, query head): merge the splits.
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ ws,
                                                           __nv_bfloat16 *__restrict__ out,
-                                                          int nsplit) {
+                                                          float *__restrict__ cor, int nsplit) {
   const int bh = blockIdx.x, dim = threadIdx.x;
   const float *rec = ws + static_cast<size_t>(bh) * nsplit * REC;
   float M = -INFINITY;
   for (int s = 0; s < nsplit; ++s) M = fmaxf(M, rec[s * REC + 2 * D + 1]);
-  float o = 0.f;
+  float o = 0.f, c = 0.f;
   if (M != -INFINITY) {
     float W = 0.f, o1 = 0.f, o2 = 0.f, sf = 0.f;
     for (int s = 0; s < nsplit; ++s) {
@@ -316,16 +316,41 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
     o1 *= inv;
     o2 *= inv;
     sf *= inv;
-    o = o1 - o2 + o1 * sf;
+    c = o2 - o1 * sf;  // the correction Sigma rho
+    o = o1 - c;
   }
   out[static_cast<size_t>(bh) * D + dim] = __float2bfloat16_rn(o);
+  if (cor != nullptr) {
+    // |correction| / |o| over the head's d values: warp sums, then 4 warps.
+    __shared__ float part[2][D / 32];
+    float csq = c * c, osq = o * o;
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+      csq += __shfl_xor_sync(0xffffffffu, csq, sh);
+      osq += __shfl_xor_sync(0xffffffffu, osq, sh);
+    }
+    if ((dim & 31) == 0) {
+      part[0][dim >> 5] = csq;
+      part[1][dim >> 5] = osq;
+    }
+    __syncthreads();
+    if (dim == 0) {
+      float cs = 0.f, os = 0.f;
+#pragma unroll
+      for (int w = 0; w < D / 32; ++w) {
+        cs += part[0][w];
+        os += part[1][w];
+      }
+      cor[bh] = os > 0.f ? sqrtf(cs) / sqrtf(os) : 0.f;
+    }
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const void *q, const void *r, const void *kcache, const void *vcache,
-                          const int *seqlens, void *out, int B, int Hq, int Hkv, int nsplit,
-                          float *workspace, unsigned *err, cudaStream_t stream) {
+                          const int *seqlens, void *out, float *cor, int B, int Hq, int Hkv,
+                          int nsplit, float *workspace, unsigned *err, cudaStream_t stream) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -371,7 +396,7 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<<<B * Hq, D, 0, stream>>>(workspace, static_cast<__nv_bfloat16 *>(out),
-                                                  nsplit);
+                                                  cor, nsplit);
   return cudaGetLastError();
 }
 

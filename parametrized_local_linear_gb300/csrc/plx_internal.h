@@ -27,13 +27,15 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
 
 // Returns cudaErrorInvalidValue if a tensor map could not be encoded.
 // L queries, the last L positions of Lk >= L keys (Lk == L: plain prefill).
+// lse and cor (|correction| / |o| per row) may be null.
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *r, void *out,
-                              float *lse, int B, int Hq, int Hkv, int L, int Lk, unsigned *err,
-                              cudaStream_t stream);
+                              float *lse, float *cor, int B, int Hq, int Hkv, int L, int Lk,
+                              unsigned *err, cudaStream_t stream);
 
+// cor ([B, Hq] fp32, |correction| / |o|) may be null.
 cudaError_t launch_decode(const void *q, const void *r, const void *kcache, const void *vcache,
-                          const int *seqlens, void *out, int B, int Hq, int Hkv, int nsplit,
-                          float *workspace, unsigned *err, cudaStream_t stream);
+                          const int *seqlens, void *out, float *cor, int B, int Hq, int Hkv,
+                          int nsplit, float *workspace, unsigned *err, cudaStream_t stream);
 
 // Fixed split-record array of the allocation-free decode: 16 MiB of fp32.
 constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;

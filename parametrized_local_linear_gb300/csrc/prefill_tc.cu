@@ -81,6 +81,7 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units
 struct PrefillArgs {
   __nv_bfloat16 *out;
   float *lse;
+  float *cor;  // optional: |correction| / |o| per row
   int Hq, Hkv, L, B, nqt, nitems;
   int Lk, qoff;  // keys per head; absolute position of query row 0 (Lk - L)
   float scale_log2;  // log2(e) / sqrt(d)
@@ -416,6 +417,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float m_used = st[row], l = st[BM + row], sg = st[2 * BM + row];
       const float inv = 1.f / l;
       const float g1 = (1.f + sg * inv) * inv;
+      // Correction (Sigma rho) = O2/l - (O1/l)(sigma/l); o = O1/l - correction.
+      const float gc = sg * inv * inv;
+      const bool want_cor = a.cor != nullptr;
+      float csq = 0.f, osq = 0.f;
       __nv_bfloat16 *orow = a.out + (static_cast<size_t>(it.zq) * a.L + grow) * D;
 #pragma unroll 1
       for (int part = 0; part < 4; ++part) {
@@ -430,8 +435,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          pk[e >> 1] = pack_bf16x2(fmaf(o1[e], g1, -o2[e] * inv), fmaf(o1[e + 1], g1, -o2[e + 1] * inv));
+        for (int e = 0; e < 32; e += 2) {
+          const float x0 = fmaf(o1[e], g1, -o2[e] * inv), x1 = fmaf(o1[e + 1], g1, -o2[e + 1] * inv);
+          pk[e >> 1] = pack_bf16x2(x0, x1);
+          if (want_cor) {
+            const float c0 = fmaf(-o1[e], gc, o2[e] * inv), c1 = fmaf(-o1[e + 1], gc, o2[e + 1] * inv);
+            csq = fmaf(c0, c0, fmaf(c1, c1, csq));
+            osq = fmaf(x0, x0, fmaf(x1, x1, osq));
+          }
+        }
         if (grow < a.L) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + part * 32);
 #pragma unroll
@@ -440,6 +452,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (a.lse != nullptr && grow < a.L)
         a.lse[static_cast<size_t>(it.zq) * a.L + grow] = (m_used + log2f(l)) * 0.6931471805599453f;
+      if (want_cor && grow < a.L)
+        a.cor[static_cast<size_t>(it.zq) * a.L + grow] = osq > 0.f ? sqrtf(csq) / sqrtf(osq) : 0.f;
     }
   }
 
@@ -466,8 +480,8 @@ bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, int L, int h
 }  // namespace
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *r, void *out,
-                              float *lse, int B, int Hq, int Hkv, int L, int Lk, unsigned *err,
-                              cudaStream_t stream) {
+                              float *lse, float *cor, int B, int Hq, int Hkv, int L, int Lk,
+                              unsigned *err, cudaStream_t stream) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -486,6 +500,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
   PrefillArgs a;
   a.out = static_cast<__nv_bfloat16 *>(out);
   a.lse = lse;
+  a.cor = cor;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.L = L;

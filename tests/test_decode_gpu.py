@@ -97,3 +97,26 @@ def test_default_split_count_is_sane():
     n = plx_decode_default_nsplit(64, 8)
     assert 1 <= n <= 256
     assert plx_decode_default_nsplit(1, 1) >= n
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv", [
+    ([1, 5, 33, 0, 200, 64], 4, 2),      # an empty sequence, a one-token one, sub-tile lengths
+    ([1000, 17, 4096], 16, 8),           # model head layout
+])
+def test_decode_cor_matches_oracle(lens, Hq, Hkv):
+    from parametrized_local_linear_gb300 import plx_decode_fwd_cor
+    from helpers import assert_cor_close
+    dev = device()
+    q, r, kc, vc, sl = inputs.decode_inputs(len(lens), Hq, Hkv, 128, lens, torch.bfloat16, 0.05,
+                                            2 * len(lens) + Hq)
+    qd, rd, kd, vd, sd = _to(dev, q, r, kc, vc, sl)
+    cor = torch.full((len(lens), Hq), float("nan"), device=dev)
+    out, _ = plx_decode_fwd_cor(qd, rd, kd, vd, sd, cor=cor)
+    plain = plx_decode_fwd(qd, rd, kd, vd, sd)
+    plx_check_device_error()
+    assert torch.equal(out, plain)  # the side output leaves o untouched
+    _, _, ref = oracle.decode(q, r, kc, vc, sl, with_cor=True)
+    assert_cor_close(cor.cpu().numpy(), ref, "decode cor")
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.all(cor[b] == 0)  # no keys: o = 0 and the ratio is defined as 0

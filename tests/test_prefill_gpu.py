@@ -146,3 +146,41 @@ def test_chunk_rejects_lq_above_lk():
     k = torch.zeros(1, 1, 32, 128, dtype=torch.bfloat16, device=dev)
     with pytest.raises(PlxError, match="Lk"):
         plx_prefill_fwd_chunk(q, k, k, q)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Lq,Lk", [
+    (1, 2, 1, 300, 300),    # plain prefill, ragged last tile
+    (2, 4, 2, 77, 333),     # chunk, offset not a multiple of the tile sizes
+    (1, 4, 2, 129, 1000),   # chunk just over one query tile
+])
+def test_bf16_cor_matches_oracle(B, Hq, Hkv, Lq, Lk):
+    from parametrized_local_linear_gb300 import plx_prefill_fwd_chunk, plx_prefill_fwd_cor
+    from helpers import assert_cor_close
+    dev = device()
+    q, k, v, r = inputs.prefill_inputs(B, Hq, Hkv, Lk, 128, torch.bfloat16, 0.05, 3 * Lq + Lk)
+    qc, rc = q[:, :, -Lq:].contiguous().to(dev), r[:, :, -Lq:].contiguous().to(dev)
+    kd, vd = k.to(dev), v.to(dev)
+    cor = torch.full(qc.shape[:3], float("nan"), device=dev)
+    out, _, _ = plx_prefill_fwd_cor(qc, kd, vd, rc, cor=cor)
+    plain, _ = plx_prefill_fwd_chunk(qc, kd, vd, rc)
+    plx_check_device_error()
+    # The side output leaves o untouched.
+    assert torch.equal(out, plain)
+    _, _, ref = oracle.prefill(qc.cpu(), k, v, rc.cpu(), with_cor=True)
+    assert_cor_close(cor.cpu().numpy(), ref, "prefill cor")
+
+
+def test_bf16_cor_full_size_sampled_rows():
+    """The 0.6B-shaped workload in the launch configuration the benchmark
+    times, ratio checked on sampled rows against the explicit-Sigma oracle."""
+    from parametrized_local_linear_gb300 import plx_prefill_fwd_cor
+    from helpers import assert_cor_close, sample_rows
+    dev = device()
+    w = inputs.PREFILL_0P6B
+    q, k, v, r = inputs.prefill_inputs_for(w)
+    _, _, cor = plx_prefill_fwd_cor(*(t.to(dev) for t in (q, k, v, r)))
+    plx_check_device_error()
+    rows = sample_rows(w.B, w.Hq, w.L, 40, 77)
+    _, _, ref = oracle.prefill(q, k, v, r, rows=rows, with_cor=True)
+    got = cor.cpu().numpy()[tuple(np.array(rows).T)]
+    assert_cor_close(got, ref, "prefill cor, full size")
