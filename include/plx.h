@@ -100,6 +100,42 @@ plx_status plx_prefill_fwd_cor(const void *q, const void *k, const void *v, cons
                                int Lk, int d, void *stream);
 
 /*
+ * Training forward: plx_prefill_fwd (Lq = Lk = L) that also saves what the
+ * backward pass needs. Extra outputs, none of which may be NULL:
+ *   lse  : fp32 [B, Hq, L]     as plx_prefill_fwd
+ *   o1   : bf16 [B, Hq, L, d]  o^SA, the softmax attention output per row
+ *   sbar : fp32 [B, Hq, L]     sum_j w_j (rho . k_j), the softmax-weighted
+ *                              mean of the probe-key products per row
+ * o is identical bit for bit to plx_prefill_fwd's.
+ */
+plx_status plx_prefill_fwd_train(const void *q, const void *k, const void *v, const void *r,
+                                 void *out, float *lse, void *o1, float *sbar, int B, int Hq,
+                                 int Hkv, int L, int d, void *stream);
+
+/*
+ * Backward pass of the causal prefill: the gradients of sum(dout * o) with
+ * respect to q, k, v and rho. The pages ("Parallax: parametrized local linear
+ * attention for language modeling") train with this layer but print no
+ * backward pass; the gradient is that of the forward definition (section
+ * "Core mechanism", output equation), streamed over the causal pairs with
+ * the forward's saved lse, o^SA and sbar.
+ *   q, r, out, o1, dout : bf16 [B, Hq, L, d]   (out, o1 from plx_prefill_fwd_train)
+ *   k, v                : bf16 [B, Hkv, L, d]
+ *   lse, sbar           : fp32 [B, Hq, L]      (from plx_prefill_fwd_train)
+ *   dq, dr              : bf16 [B, Hq, L, d]   written
+ *   dk, dv              : bf16 [B, Hkv, L, d]  written (summed over each
+ *                                              kv head's query heads)
+ * d must be 128; every pointer non-NULL and 16-byte aligned. Allocates a
+ * stream-ordered workspace of B * Hq * round_up(L, 64) * 16 bytes
+ * (cudaMallocAsync / cudaFreeAsync on `stream`). Deterministic: no atomics,
+ * every output row is written by one thread block.
+ */
+plx_status plx_prefill_bwd(const void *q, const void *k, const void *v, const void *r,
+                           const void *out, const void *o1, const float *lse, const float *sbar,
+                           const void *dout, void *dq, void *dk, void *dv, void *dr, int B, int Hq,
+                           int Hkv, int L, int d, void *stream);
+
+/*
  * Causal prefill in fp32 (CUDA cores, fp32 arithmetic throughout). Same
  * arguments and layouts as plx_prefill_fwd with float tensors; d in {64, 128}.
  * This is the exact-arithmetic path used to check parity at 1e-5 relative error.

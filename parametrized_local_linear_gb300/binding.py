@@ -31,6 +31,8 @@ SIGNATURES = {
     "plx_prefill_fwd_f32": (_i, [_vp] * 6 + [_i] * 5 + [_vp]),
     "plx_prefill_fwd_chunk": (_i, [_vp] * 6 + [_i] * 6 + [_vp]),
     "plx_prefill_fwd_cor": (_i, [_vp] * 7 + [_i] * 6 + [_vp]),
+    "plx_prefill_fwd_train": (_i, [_vp] * 8 + [_i] * 5 + [_vp]),
+    "plx_prefill_bwd": (_i, [_vp] * 13 + [_i] * 5 + [_vp]),
     "plx_decode_fwd": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
     "plx_decode_fwd_ex": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
     "plx_decode_fwd_noalloc": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
@@ -181,6 +183,71 @@ def _prefill_chunk(q, k, v, r, out, lse, cor, stream):
                                            Lk, d, _stream(stream, dev))
     _check(st)
     return out, lse, cor
+
+
+def plx_prefill_fwd_train(q, k, v, r, out=None, lse=None, o1=None, sbar=None, stream=None):
+    """Training forward (see include/plx.h): returns (out, lse, o1, sbar), the
+    last three being what plx_prefill_bwd needs."""
+    _need(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("r", r)):
+        _need(t, name, torch.bfloat16, 4, dev)
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(r.shape) != tuple(q.shape) or tuple(k.shape) != (B, Hkv, L, d) or v.shape != k.shape:
+        raise ValueError("r must match q; k and v must be [B, Hkv, L, d]")
+    out = torch.empty_like(q) if out is None else out
+    o1 = torch.empty_like(q) if o1 is None else o1
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=dev) if lse is None else lse
+    sbar = torch.empty((B, Hq, L), dtype=torch.float32, device=dev) if sbar is None else sbar
+    for name, t in (("out", out), ("o1", o1)):
+        _need(t, name, torch.bfloat16, 4, dev)
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} must have the shape of q")
+    for name, t in (("lse", lse), ("sbar", sbar)):
+        _need(t, name, torch.float32, 3, dev)
+        if tuple(t.shape) != (B, Hq, L):
+            raise ValueError(f"{name} must be [B, Hq, L]")
+    with torch.cuda.device(dev):
+        st = lib().plx_prefill_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
+                                         out.data_ptr(), lse.data_ptr(), o1.data_ptr(),
+                                         sbar.data_ptr(), B, Hq, Hkv, L, d, _stream(stream, dev))
+    _check(st)
+    return out, lse, o1, sbar
+
+
+def plx_prefill_bwd(q, k, v, r, out, o1, lse, sbar, dout, dq=None, dk=None, dv=None, dr=None,
+                    stream=None):
+    """Backward of the causal prefill (see include/plx.h). Returns
+    (dq, dk, dv, dr), bf16, shaped like q, k, v, r."""
+    _need(q, "q", torch.bfloat16, 4)
+    dev = q.device
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 4, dev)
+        if tuple(t.shape) != (B, Hkv, L, d):
+            raise ValueError(f"{name} must be [B, Hkv, L, d]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dr = torch.empty_like(q) if dr is None else dr
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, like in (("r", r, q), ("out", out, q), ("o1", o1, q), ("dout", dout, q),
+                          ("dq", dq, q), ("dr", dr, q), ("dk", dk, k), ("dv", dv, k)):
+        _need(t, name, torch.bfloat16, 4, dev)
+        if tuple(t.shape) != tuple(like.shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(like.shape)}")
+    for name, t in (("lse", lse), ("sbar", sbar)):
+        _need(t, name, torch.float32, 3, dev)
+        if tuple(t.shape) != (B, Hq, L):
+            raise ValueError(f"{name} must be [B, Hq, L]")
+    with torch.cuda.device(dev):
+        st = lib().plx_prefill_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), r.data_ptr(),
+                                   out.data_ptr(), o1.data_ptr(), lse.data_ptr(), sbar.data_ptr(),
+                                   dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                   dr.data_ptr(), B, Hq, Hkv, L, d, _stream(stream, dev))
+    _check(st)
+    return dq, dk, dv, dr
 
 
 def plx_prefill_fwd_f32(q, k, v, r, out=None, lse=None, stream=None):

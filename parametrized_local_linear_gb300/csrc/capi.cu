@@ -136,19 +136,20 @@ extern "C" {
 namespace {
 
 plx_status prefill_bf16(const char *fn, const void *q, const void *k, const void *v, const void *r,
-                        void *out, float *lse, float *cor, int B, int Hq, int Hkv, int Lq, int Lk,
-                        int d, void *stream) {
+                        void *out, float *lse, float *cor, void *o1, float *sbar, int B, int Hq,
+                        int Hkv, int Lq, int Lk, int d, void *stream) {
   if (!q || !k || !v || !r || !out) return fail(PLX_ERR_INVALID_ARG, "%s: null tensor pointer", fn);
   plx_status s = check_common(fn, B, Hq, Hkv, Lq, d);
   if (s) return s;
   if (Lk < Lq) return fail(PLX_ERR_INVALID_ARG, "%s: Lk (%d) must be >= Lq (%d)", fn, Lk, Lq);
   if (d != 128) return fail(PLX_ERR_UNSUPPORTED, "%s: head dim %d (only 128)", fn, d);
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(r) || !aligned16(out))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(r) || !aligned16(out) ||
+      !aligned16(o1))
     return fail(PLX_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", fn);
   if (static_cast<long long>(Lq + 127) / 128 * Hq * B > 0x7fffffffLL ||
       static_cast<long long>(B) * Hq > 0x7fffffff)
     return fail(PLX_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
-  return finish_launch(plx::launch_prefill_tc(q, k, v, r, out, lse, cor, B, Hq, Hkv, Lq, Lk,
+  return finish_launch(plx::launch_prefill_tc(q, k, v, r, out, lse, cor, o1, sbar, B, Hq, Hkv, Lq, Lk,
                                               plx::device_error_word(),
                                               static_cast<cudaStream_t>(stream)),
                        fn);
@@ -159,16 +160,52 @@ plx_status prefill_bf16(const char *fn, const void *q, const void *k, const void
 plx_status plx_prefill_fwd_chunk(const void *q, const void *k, const void *v, const void *r,
                                  void *out, float *lse, int B, int Hq, int Hkv, int Lq, int Lk,
                                  int d, void *stream) {
-  return prefill_bf16("plx_prefill_fwd", q, k, v, r, out, lse, nullptr, B, Hq, Hkv, Lq, Lk, d,
-                      stream);
+  return prefill_bf16("plx_prefill_fwd", q, k, v, r, out, lse, nullptr, nullptr, nullptr, B, Hq, Hkv,
+                      Lq, Lk, d, stream);
 }
 
 plx_status plx_prefill_fwd_cor(const void *q, const void *k, const void *v, const void *r,
                                void *out, float *lse, float *cor, int B, int Hq, int Hkv, int Lq,
                                int Lk, int d, void *stream) {
   if (!cor) return fail(PLX_ERR_INVALID_ARG, "plx_prefill_fwd_cor: null cor pointer");
-  return prefill_bf16("plx_prefill_fwd_cor", q, k, v, r, out, lse, cor, B, Hq, Hkv, Lq, Lk, d,
-                      stream);
+  return prefill_bf16("plx_prefill_fwd_cor", q, k, v, r, out, lse, cor, nullptr, nullptr, B, Hq, Hkv,
+                      Lq, Lk, d, stream);
+}
+
+plx_status plx_prefill_fwd_train(const void *q, const void *k, const void *v, const void *r,
+                                 void *out, float *lse, void *o1, float *sbar, int B, int Hq,
+                                 int Hkv, int L, int d, void *stream) {
+  const char *fn = "plx_prefill_fwd_train";
+  if (!lse || !o1 || !sbar) return fail(PLX_ERR_INVALID_ARG, "%s: null lse, o1 or sbar", fn);
+  return prefill_bf16(fn, q, k, v, r, out, lse, nullptr, o1, sbar, B, Hq, Hkv, L, L, d, stream);
+}
+
+plx_status plx_prefill_bwd(const void *q, const void *k, const void *v, const void *r,
+                           const void *out, const void *o1, const float *lse, const float *sbar,
+                           const void *dout, void *dq, void *dk, void *dv, void *dr, int B, int Hq,
+                           int Hkv, int L, int d, void *stream) {
+  const char *fn = "plx_prefill_bwd";
+  if (!q || !k || !v || !r || !out || !o1 || !lse || !sbar || !dout || !dq || !dk || !dv || !dr)
+    return fail(PLX_ERR_INVALID_ARG, "%s: null pointer", fn);
+  plx_status s = check_common(fn, B, Hq, Hkv, L, d);
+  if (s) return s;
+  if (d != 128) return fail(PLX_ERR_UNSUPPORTED, "%s: head dim %d (only 128)", fn, d);
+  const void *ptrs[] = {q, k, v, r, out, o1, dout, dq, dk, dv, dr};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return fail(PLX_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", fn);
+  if (static_cast<long long>(L + 127) / 128 * Hq * B > 0x7fffffffLL)
+    return fail(PLX_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void *ws = nullptr;
+  const size_t need = plx::prefill_bwd_stats_count(B, Hq, L) * 4 * sizeof(float);
+  cudaError_t e = cudaMallocAsync(&ws, need, st);
+  if (e != cudaSuccess) return cuda_fail(e, "plx_prefill_bwd: workspace allocation");
+  e = plx::launch_prefill_bwd(q, k, v, r, out, o1, lse, sbar, dout, dq, dk, dv, dr, B, Hq, Hkv, L,
+                              ws, plx::device_error_word(), st);
+  cudaError_t e2 = cudaFreeAsync(ws, st);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  if (e2 != cudaSuccess) return cuda_fail(e2, "plx_prefill_bwd: workspace release");
+  return PLX_OK;
 }
 
 plx_status plx_prefill_fwd(const void *q, const void *k, const void *v, const void *r, void *out,

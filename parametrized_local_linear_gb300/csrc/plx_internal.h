@@ -26,11 +26,26 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
                                unsigned *err, cudaStream_t stream);
 
 // Returns cudaErrorInvalidValue if a tensor map could not be encoded.
+// 3-D bf16 tensor map over [heads][L][128] with 128-byte swizzle and boxes
+// of box_rows x 64 elements (zero fill past L).
+bool make_head_rows_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, int L, int heads,
+                        int box_rows);
+
 // L queries, the last L positions of Lk >= L keys (Lk == L: plain prefill).
-// lse and cor (|correction| / |o| per row) may be null.
+// lse, cor (|correction| / |o| per row), o1 (bf16 o^SA per row) and sbar
+// (sigma / l per row) may each be null.
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *r, void *out,
-                              float *lse, float *cor, int B, int Hq, int Hkv, int L, int Lk,
-                              unsigned *err, cudaStream_t stream);
+                              float *lse, float *cor, void *o1, float *sbar, int B, int Hq, int Hkv,
+                              int L, int Lk, unsigned *err, cudaStream_t stream);
+
+// Backward of the causal prefill (Lq == Lk == L, d = 128, bf16). stats is a
+// workspace of B * Hq * round_up(L, 64) float4 records.
+size_t prefill_bwd_stats_count(int B, int Hq, int L);
+cudaError_t launch_prefill_bwd(const void *q, const void *k, const void *v, const void *r,
+                               const void *out, const void *o1, const float *lse,
+                               const float *sbar, const void *dout, void *dq, void *dk, void *dv,
+                               void *dr, int B, int Hq, int Hkv, int L, void *stats, unsigned *err,
+                               cudaStream_t stream);
 
 // cor ([B, Hq] fp32, |correction| / |o|) may be null.
 cudaError_t launch_decode(const void *q, const void *r, const void *kcache, const void *vcache,

@@ -1,0 +1,683 @@
+// Backward pass of the causal Parallax prefill on the tcgen05 tensor cores
+// (bf16 operands, fp32 accumulation in TMEM, TMA loads), d = 128.
+//
+// The pages ("Parallax: parametrized local linear attention for language
+// modeling", section "Core mechanism" for the forward, section
+// "Experimental results" for the training runs) print no backward pass. With
+// w the causal softmax weights of query i, t_j = rho_i . k_j,
+// sbar = sum_j w_j t_j and c_j = 1 + sbar - t_j, the forward is
+// o = sum_j w_j c_j v_j. For an output gradient g, with u_j = g . v_j,
+// a = g . o^SA and D = g . o + a sbar, differentiating gives
+//   dv_j   += w_j c_j g
+//   dt_j    = w_j (a - u_j)
+//   ds_j    = w_j (c_j u_j + a t_j - D)        (score gradient)
+//   dq      = tau sum_j ds_j k_j,   drho = sum_j dt_j k_j
+//   dk_j   += tau ds_j q + dt_j rho
+// (the tests check this form against autograd through the explicit
+// covariance). The forward saves lse, o^SA and sbar per row; a small kernel
+// turns them into one record per row {lse log2 e, 1 + sbar, a, D}.
+//
+// Two kernels then stream the causal pairs, each with the same TMEM plan
+// (512 columns): S [0,64) T [64,128) U [128,192) packed bf16 score and probe
+// gradients [192,224) [224,256), two fp32 accumulators [256,384) [384,512).
+//   bwd_dq_kernel: one CTA per 128 query rows; per 64-key tile
+//     S = Q K^T, T = R K^T, U = dO V^T; dS, dT; dQ += dS K, dR += dT K.
+//   bwd_dkv_kernel: one CTA per 128 keys of one kv head, over every query
+//     head of its group and every 64-query tile at or after the keys;
+//     S^T = K Q^T, T^T = K R^T, U^T = V dO^T; then dV += (w c)^T dO and
+//     dK += dS^T Q + dT^T R.
+// Neither kernel needs atomics: each output row is owned by one CTA. The
+// elementwise warps release S, T and U as soon as they have loaded them
+// (stu_free), so the next tile's score UMMAs run under the elementwise work
+// and the current tile's gradient UMMAs. 10 warps: 0 TMA producer, 1 TMEM
+// allocator + UMMA issuer, 2..9 elementwise (two warps per TMEM lane quarter,
+// each taking half of the tile's 64 columns; there is no row reduction, so
+// the columns split freely).
+#include <math.h>
+
+#include "plx_device.cuh"
+#include "plx_internal.h"
+
+namespace plx {
+namespace {
+
+constexpr int D = 128;
+constexpr int THREADS = 32 * 10;
+constexpr int NEW = 256;                  // elementwise threads
+constexpr uint32_t COL_S = 0, COL_T = 64, COL_U = 128, COL_GS = 192, COL_GT = 224;
+constexpr uint32_t COL_ACC0 = 256, COL_ACC1 = 384;
+constexpr int STAT_ROWS = 64;             // stats rows are padded to this multiple
+
+struct BwdArgs {
+  __nv_bfloat16 *g0, *g1;  // dq, dr (dq kernel) or dv, dk (dkv kernel)
+  const float4 *stats;     // [B * Hq][Lpad] {lse log2 e, 1 + sbar, a, D}
+  int B, Hq, Hkv, L, Lpad;
+  float scale_log2, tau;
+  unsigned *err;
+};
+
+// ---------------------------------------------------------------- per-row records
+// One warp per (padded) row: a = g . o^SA, D = g . o + a sbar.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(
+    const __nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *__restrict__ o1,
+    const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ lse,
+    const float *__restrict__ sbar, float4 *__restrict__ stats, int L, int Lpad, long long nrows) {
+  const long long p = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (p >= nrows) return;
+  const long long zh = p / Lpad;
+  const int i = static_cast<int>(p - zh * Lpad);
+  if (i >= L) {
+    // Padding rows: weight 2^-inf = 0 for every key.
+    if (lane == 0) stats[p] = make_float4(INFINITY, 1.f, 0.f, 0.f);
+    return;
+  }
+  const long long row = zh * L + i;
+  const size_t off = static_cast<size_t>(row) * D + lane * 4;
+  const uint2 gv = *reinterpret_cast<const uint2 *>(dout + off);
+  const uint2 ov = *reinterpret_cast<const uint2 *>(out + off);
+  const uint2 av = *reinterpret_cast<const uint2 *>(o1 + off);
+  const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gv.x));
+  const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gv.y));
+  const float2 o0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ov.x));
+  const float2 o1v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ov.y));
+  const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&av.x));
+  const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&av.y));
+  float go = g0.x * o0.x + g0.y * o0.y + g1.x * o1v.x + g1.y * o1v.y;
+  float ga = g0.x * a0.x + g0.y * a0.y + g1.x * a1.x + g1.y * a1.y;
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) {
+    go += __shfl_xor_sync(0xffffffffu, go, sh);
+    ga += __shfl_xor_sync(0xffffffffu, ga, sh);
+  }
+  if (lane == 0) {
+    const float sb = sbar[row];
+    stats[p] = make_float4(lse[row] * 1.4426950408889634f, 1.f + sb, ga, fmaf(ga, sb, go));
+  }
+}
+
+// Gradients of two columns of one (query, key) row pair block: inputs raw
+// scores s, probe products t, u = g . v; outputs tau * ds, dt and w c.
+struct Grad2 {
+  uint32_t gs, gt, pc;
+};
+__device__ __forceinline__ Grad2 grad_pair(float s0, float s1, float t0, float t1, float u0, float u1,
+                                           bool m0, bool m1, float4 st0, float4 st1, float c,
+                                           float tau) {
+  // st = {lse log2 e, 1 + sbar, a, D}
+  float w0 = fast_exp2(fmaf(s0, c, -st0.x));
+  float w1 = fast_exp2(fmaf(s1, c, -st1.x));
+  w0 = m0 ? 0.f : w0;
+  w1 = m1 ? 0.f : w1;
+  const float c0 = st0.y - t0, c1 = st1.y - t1;
+  const float d0 = fmaf(c0, u0, fmaf(st0.z, t0, -st0.w));
+  const float d1 = fmaf(c1, u1, fmaf(st1.z, t1, -st1.w));
+  Grad2 r;
+  r.gs = pack_bf16x2(w0 * d0 * tau, w1 * d1 * tau);
+  r.gt = pack_bf16x2(w0 * (st0.z - u0), w1 * (st1.z - u1));
+  r.pc = pack_bf16x2(w0 * c0, w1 * c1);
+  return r;
+}
+
+// Reads 128 fp32 TMEM columns [col, col + 64) of this thread's lane as two
+// 32-column pieces, converts to bf16 and stores them at dst (64 values).
+__device__ __forceinline__ void store_acc_half(uint32_t taddr, __nv_bfloat16 *dst, bool valid) {
+#pragma unroll 1
+  for (int part = 0; part < 2; ++part) {
+    float v[32];
+    tmem_ld32(taddr + part * 32, v);
+    tmem_wait_ld();
+    if (valid) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(v[e], v[e + 1]);
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + part * 32);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+    }
+  }
+}
+
+// =================================================================== dQ, dR
+namespace qk {
+constexpr int BM = 128;                        // query rows per CTA
+constexpr int BN = 64;                         // keys per tile
+constexpr int NST = 3;                         // K / V ring stages
+constexpr int HALF_Q = BM * 64 * 2;            // 16 KB
+constexpr int HALF_KV = BN * 64 * 2;           // 8 KB
+constexpr int TILE_KV = 2 * HALF_KV;
+constexpr int OFF_Q = 0, OFF_R = 2 * HALF_Q, OFF_DO = 4 * HALF_Q;
+constexpr int OFF_K = 6 * HALF_Q;              // 98304
+constexpr int OFF_V = OFF_K + NST * TILE_KV;   // 147456
+constexpr int OFF_BAR = OFF_V + NST * TILE_KV; // 196608
+constexpr int NBAR = 1 + 4 * NST + 6;
+constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
+}  // namespace qk
+
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
+                  const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
+  using namespace qk;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+  uint64_t *q_full = bars;              // Q, R, dO loaded
+  uint64_t *k_full = bars + 1;
+  uint64_t *k_empty = k_full + NST;     // dQ / dR UMMAs of the tile done
+  uint64_t *v_full = k_empty + NST;
+  uint64_t *v_empty = v_full + NST;     // U UMMAs of the tile done
+  uint64_t *stu_full = v_empty + NST;   // S, T, U of the tile in TMEM
+  uint64_t *stu_free = stu_full + 1;    // count 256: S, T, U loaded by every thread
+  uint64_t *gs_full = stu_free + 1;     // count 256: dS, dT written
+  uint64_t *acc_done = gs_full + 1;     // dQ / dR UMMAs of the tile done
+  uint64_t *acc_full = acc_done + 1;    // every UMMA done (epilogue)
+  uint64_t *drain = acc_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqt = (a.L + BM - 1) / BM, per = a.B * a.Hq;
+  const int o = blockIdx.x;
+  const int qt = nqt - 1 - o / per, rem = o % per;
+  const int h = rem % a.Hq, b = rem / a.Hq;
+  const int zq = b * a.Hq + h, zk = b * a.Hkv + h / (a.Hq / a.Hkv);
+  const int q0 = qt * BM;
+  const int n = (min(q0 + BM, a.L) + BN - 1) / BN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(q_full), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
+    }
+    mbar_init(smem_u32(stu_full), 1);
+    mbar_init(smem_u32(stu_free), NEW);
+    mbar_init(smem_u32(gs_full), NEW);
+    mbar_init(smem_u32(acc_done), 1);
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_r);
+    prefetch_tensormap(&tm_do);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const Abort ab{abort_flag, a.err};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint32_t qb = smem_u32(q_full);
+      mbar_arrive_expect_tx(qb, 6 * HALF_Q);
+      tma_load_3d(smem_u32(smem + OFF_Q), &tm_q, 0, q0, zq, qb);
+      tma_load_3d(smem_u32(smem + OFF_Q + HALF_Q), &tm_q, 64, q0, zq, qb);
+      tma_load_3d(smem_u32(smem + OFF_R), &tm_r, 0, q0, zq, qb);
+      tma_load_3d(smem_u32(smem + OFF_R + HALF_Q), &tm_r, 64, q0, zq, qb);
+      tma_load_3d(smem_u32(smem + OFF_DO), &tm_do, 0, q0, zq, qb);
+      tma_load_3d(smem_u32(smem + OFF_DO + HALF_Q), &tm_do, 64, q0, zq, qb);
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < n; ++j) {
+        const int st = j % NST;
+        if (j >= NST && !mbar_wait(smem_u32(&k_empty[st]), ((j / NST) - 1) & 1, ab)) break;
+        const uint32_t kf = smem_u32(&k_full[st]);
+        mbar_arrive_expect_tx(kf, TILE_KV);
+        const uint32_t kb = smem_u32(smem + OFF_K + st * TILE_KV);
+        tma_load_3d(kb, &tm_k, 0, j * BN, zk, kf);
+        tma_load_3d(kb + HALF_KV, &tm_k, 64, j * BN, zk, kf);
+        k_issued = j + 1;
+        if (j >= NST && !mbar_wait(smem_u32(&v_empty[st]), ((j / NST) - 1) & 1, ab)) break;
+        const uint32_t vf = smem_u32(&v_full[st]);
+        mbar_arrive_expect_tx(vf, TILE_KV);
+        const uint32_t vb = smem_u32(smem + OFF_V + st * TILE_KV);
+        tma_load_3d(vb, &tm_v, 0, j * BN, zk, vf);
+        tma_load_3d(vb + HALF_KV, &tm_v, 64, j * BN, zk, vf);
+        v_issued = j + 1;
+      }
+      if (ab.raised()) {
+        mbar_wait_drain(qb, 0);
+        for (int j = max(0, k_issued - NST); j < k_issued; ++j)
+          mbar_wait_drain(smem_u32(&k_full[j % NST]), (j / NST) & 1);
+        for (int j = max(0, v_issued - NST); j < v_issued; ++j)
+          mbar_wait_drain(smem_u32(&v_full[j % NST]), (j / NST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- UMMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
+      constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, 1);
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+      const uint64_t rdesc = smem_desc_sw128(smem_u32(smem + OFF_R), 16, 1024);
+      const uint64_t odesc = smem_desc_sw128(smem_u32(smem + OFF_DO), 16, 1024);
+      const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
+      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + OFF_V), 16, 1024);
+      const uint64_t kmn0 = smem_desc_sw128(smem_u32(smem + OFF_K), HALF_KV, 1024);
+      bool ok = mbar_wait(smem_u32(q_full), 0, ab);
+      // S, T, U of tile j (K-major operands on both sides).
+      auto issue_stu = [&](int j) -> bool {
+        const int st = j % NST, ph = (j / NST) & 1;
+        if (!mbar_wait(smem_u32(&k_full[st]), ph, ab)) return false;
+        if (!mbar_wait(smem_u32(&v_full[st]), ph, ab)) return false;
+        tc_fence_after();
+        const uint64_t kd = kdesc0 + st * (TILE_KV >> 4), vd = vdesc0 + st * (TILE_KV >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ao = (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2;
+          const uint32_t bo = (ks >> 2) * (HALF_KV >> 4) + (ks & 3) * 2;
+          umma_ss(tbase + COL_S, qdesc + ao, kd + bo, idesc_s, ks > 0);
+          umma_ss(tbase + COL_T, rdesc + ao, kd + bo, idesc_s, ks > 0);
+          umma_ss(tbase + COL_U, odesc + ao, vd + bo, idesc_s, ks > 0);
+        }
+        umma_commit(smem_u32(stu_full));
+        umma_commit(smem_u32(&v_empty[st]));
+        return true;
+      };
+      ok = ok && issue_stu(0);
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          // S, T, U of tile j are in registers once stu_free completes.
+          if (!mbar_wait(smem_u32(stu_free), j & 1, ab) || !issue_stu(j + 1)) break;
+        }
+        if (!mbar_wait(smem_u32(gs_full), j & 1, ab)) break;
+        tc_fence_after();
+        const int st = j % NST;
+        const uint64_t km = kmn0 + st * (TILE_KV >> 4);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          umma_ts(tbase + COL_ACC0, tbase + COL_GS + ks * 8, km + ks * (2048 >> 4), idesc_g, (j > 0 || ks > 0));
+          umma_ts(tbase + COL_ACC1, tbase + COL_GT + ks * 8, km + ks * (2048 >> 4), idesc_g, (j > 0 || ks > 0));
+        }
+        umma_commit(smem_u32(acc_done));
+        umma_commit(smem_u32(&k_empty[st]));
+      }
+      umma_commit(smem_u32(acc_full));
+      umma_commit(smem_u32(drain));
+      mbar_wait_drain(smem_u32(drain), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int qw = warp & 3, hf = (warp - 2) >> 2;
+    const int row = qw * 32 + lane, grow = q0 + row;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(qw * 32) << 16);
+    const float4 st = grow < a.L ? a.stats[static_cast<size_t>(zq) * a.Lpad + grow]
+                                 : make_float4(INFINITY, 1.f, 0.f, 0.f);
+    const float c = a.scale_log2, tau = a.tau;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      ok = mbar_wait(smem_u32(stu_full), j & 1, ab);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float s[32], t[32], u[32];
+      tmem_ld32(tl + COL_S + 32 * hf, s);
+      tmem_ld32(tl + COL_T + 32 * hf, t);
+      tmem_ld32(tl + COL_U + 32 * hf, u);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(stu_free));
+      const int kbase = j * BN + 32 * hf;
+      uint32_t gs[16], gt[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const Grad2 g2 = grad_pair(s[e], s[e + 1], t[e], t[e + 1], u[e], u[e + 1], kbase + e > grow,
+                                   kbase + e + 1 > grow, st, st, c, tau);
+        gs[e >> 1] = g2.gs;
+        gt[e >> 1] = g2.gt;
+      }
+      if (j > 0) {
+        // The previous tile's dQ / dR UMMAs read the gradient columns.
+        ok = mbar_wait(smem_u32(acc_done), (j - 1) & 1, ab);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      tmem_st16(tl + COL_GS + 16 * hf, gs);
+      tmem_st16(tl + COL_GT + 16 * hf, gt);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(gs_full));
+    }
+    if (ok) {
+      ok = mbar_wait(smem_u32(acc_full), 0, ab);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const bool valid = grow < a.L;
+        const size_t ro = (static_cast<size_t>(zq) * a.L + (valid ? grow : 0)) * D + 64 * hf;
+        store_acc_half(tl + COL_ACC0 + 64 * hf, a.g0 + ro, valid);
+        store_acc_half(tl + COL_ACC1 + 64 * hf, a.g1 + ro, valid);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// =================================================================== dK, dV
+namespace kv {
+constexpr int BM = 128;                        // keys per CTA
+constexpr int BN = 64;                         // queries per step
+constexpr int NST = 3;                         // Q / R / dO ring stages
+constexpr int HALF_K = BM * 64 * 2;            // 16 KB
+constexpr int HALF_Q = BN * 64 * 2;            // 8 KB
+constexpr int TILE_Q = 2 * HALF_Q;             // 16 KB
+constexpr int STAGE = 3 * TILE_Q;              // Q, R, dO
+constexpr int OFF_K = 0, OFF_V = 2 * HALF_K;
+constexpr int OFF_P = 4 * HALF_K;              // 65536: (w c)^T tile, 128 keys x 64 queries bf16
+constexpr int OFF_STG = OFF_P + BM * BN * 2;   // 81920
+constexpr int OFF_BAR = OFF_STG + NST * STAGE; // 229376
+constexpr int NBAR = 1 + 2 * NST + 6;
+constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
+}  // namespace kv
+
+__global__ void __launch_bounds__(THREADS, 1)
+    bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
+                   const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
+  using namespace kv;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+  uint64_t *kv_full = bars;             // K and V blocks loaded
+  uint64_t *q_full = bars + 1;          // [NST] Q, R, dO of a step loaded
+  uint64_t *q_empty = q_full + NST;     // [NST] the step's dV / dK UMMAs done
+  uint64_t *stu_full = q_empty + NST;
+  uint64_t *stu_free = stu_full + 1;    // count 256
+  uint64_t *gs_full = stu_free + 1;     // count 256: (w c)^T in smem, dS^T / dT^T in TMEM
+  uint64_t *acc_done = gs_full + 1;
+  uint64_t *acc_full = acc_done + 1;
+  uint64_t *drain = acc_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = a.B * a.Hkv, G = a.Hq / a.Hkv;
+  const int o = blockIdx.x;
+  const int kb = o / per, rem = o % per;  // key blocks in ascending order: longest first
+  const int kvh = rem % a.Hkv, b = rem / a.Hkv;
+  const int zk = b * a.Hkv + kvh;
+  const int k0 = kb * BM;
+  const int qt_lo = k0 / BN, nqt = (a.L + BN - 1) / BN;
+  const int per_head = nqt - qt_lo;
+  const int n = G * per_head;             // steps: every query head of the group x query tiles
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(kv_full), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(smem_u32(&q_full[s]), 1);
+      mbar_init(smem_u32(&q_empty[s]), 1);
+    }
+    mbar_init(smem_u32(stu_full), 1);
+    mbar_init(smem_u32(stu_free), NEW);
+    mbar_init(smem_u32(gs_full), NEW);
+    mbar_init(smem_u32(acc_done), 1);
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_r);
+    prefetch_tensormap(&tm_do);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const Abort ab{abort_flag, a.err};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint32_t kvb = smem_u32(kv_full);
+      mbar_arrive_expect_tx(kvb, 4 * HALF_K);
+      tma_load_3d(smem_u32(smem + OFF_K), &tm_k, 0, k0, zk, kvb);
+      tma_load_3d(smem_u32(smem + OFF_K + HALF_K), &tm_k, 64, k0, zk, kvb);
+      tma_load_3d(smem_u32(smem + OFF_V), &tm_v, 0, k0, zk, kvb);
+      tma_load_3d(smem_u32(smem + OFF_V + HALF_K), &tm_v, 64, k0, zk, kvb);
+      int issued = 0;
+      for (int s = 0; s < n; ++s) {
+        const int st = s % NST;
+        if (s >= NST && !mbar_wait(smem_u32(&q_empty[st]), ((s / NST) - 1) & 1, ab)) break;
+        const int zq = b * a.Hq + kvh * G + s / per_head, y = (qt_lo + s % per_head) * BN;
+        const uint32_t qf = smem_u32(&q_full[st]);
+        const uint32_t base = smem_u32(smem + OFF_STG + st * STAGE);
+        mbar_arrive_expect_tx(qf, STAGE);
+        tma_load_3d(base, &tm_q, 0, y, zq, qf);
+        tma_load_3d(base + HALF_Q, &tm_q, 64, y, zq, qf);
+        tma_load_3d(base + TILE_Q, &tm_r, 0, y, zq, qf);
+        tma_load_3d(base + TILE_Q + HALF_Q, &tm_r, 64, y, zq, qf);
+        tma_load_3d(base + 2 * TILE_Q, &tm_do, 0, y, zq, qf);
+        tma_load_3d(base + 2 * TILE_Q + HALF_Q, &tm_do, 64, y, zq, qf);
+        issued = s + 1;
+      }
+      if (ab.raised()) {
+        mbar_wait_drain(kvb, 0);
+        for (int s = max(0, issued - NST); s < issued; ++s)
+          mbar_wait_drain(smem_u32(&q_full[s % NST]), (s / NST) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- UMMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
+      constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, 1);
+      const uint64_t kdesc = smem_desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
+      const uint64_t vdesc = smem_desc_sw128(smem_u32(smem + OFF_V), 16, 1024);
+      const uint64_t pdesc = smem_desc_sw128(smem_u32(smem + OFF_P), 16, 1024);
+      const uint64_t stg_k = smem_desc_sw128(smem_u32(smem + OFF_STG), 16, 1024);        // K-major view
+      const uint64_t stg_mn = smem_desc_sw128(smem_u32(smem + OFF_STG), HALF_Q, 1024);   // MN-major view
+      bool ok = mbar_wait(smem_u32(kv_full), 0, ab);
+      auto issue_stu = [&](int s) -> bool {
+        const int st = s % NST;
+        if (!mbar_wait(smem_u32(&q_full[st]), (s / NST) & 1, ab)) return false;
+        tc_fence_after();
+        const uint64_t qd = stg_k + st * (STAGE >> 4);
+        const uint64_t rd = qd + (TILE_Q >> 4), od = qd + 2 * (TILE_Q >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ao = (ks >> 2) * (HALF_K >> 4) + (ks & 3) * 2;
+          const uint32_t bo = (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2;
+          umma_ss(tbase + COL_S, kdesc + ao, qd + bo, idesc_s, ks > 0);
+          umma_ss(tbase + COL_T, kdesc + ao, rd + bo, idesc_s, ks > 0);
+          umma_ss(tbase + COL_U, vdesc + ao, od + bo, idesc_s, ks > 0);
+        }
+        umma_commit(smem_u32(stu_full));
+        return true;
+      };
+      ok = ok && issue_stu(0);
+      for (int s = 0; ok && s < n; ++s) {
+        if (s + 1 < n) {
+          if (!mbar_wait(smem_u32(stu_free), s & 1, ab) || !issue_stu(s + 1)) break;
+        }
+        if (!mbar_wait(smem_u32(gs_full), s & 1, ab)) break;
+        tc_fence_after();
+        const int st = s % NST;
+        const uint64_t qm = stg_mn + st * (STAGE >> 4);
+        const uint64_t rm = qm + (TILE_Q >> 4), om = qm + 2 * (TILE_Q >> 4);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          // dV += (w c)^T dO;  dK += (tau dS)^T Q + dT^T R.
+          umma_ss(tbase + COL_ACC0, pdesc + ks * 2, om + ks * (2048 >> 4), idesc_g, (s > 0 || ks > 0));
+          umma_ts(tbase + COL_ACC1, tbase + COL_GS + ks * 8, qm + ks * (2048 >> 4), idesc_g, (s > 0 || ks > 0));
+          umma_ts(tbase + COL_ACC1, tbase + COL_GT + ks * 8, rm + ks * (2048 >> 4), idesc_g, 1);
+        }
+        umma_commit(smem_u32(acc_done));
+        umma_commit(smem_u32(&q_empty[st]));
+      }
+      umma_commit(smem_u32(acc_full));
+      umma_commit(smem_u32(drain));
+      mbar_wait_drain(smem_u32(drain), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int qw = warp & 3, hf = (warp - 2) >> 2;
+    const int row = qw * 32 + lane, krow = k0 + row;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(qw * 32) << 16);
+    // This thread's row of the (w c)^T tile: 128-byte rows, 16-byte chunks
+    // XOR-swizzled by the row index within each 8-row group (SW128, K-major).
+    uint8_t *prow = smem + OFF_P + (row >> 3) * 1024 + (row & 7) * 128;
+    const float c = a.scale_log2, tau = a.tau;
+    bool ok = true;
+    for (int s = 0; s < n; ++s) {
+      ok = mbar_wait(smem_u32(stu_full), s & 1, ab);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      float sv[32], tv[32], uv[32];
+      tmem_ld32(tl + COL_S + 32 * hf, sv);
+      tmem_ld32(tl + COL_T + 32 * hf, tv);
+      tmem_ld32(tl + COL_U + 32 * hf, uv);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(stu_free));
+      const int zq = b * a.Hq + kvh * G + s / per_head;
+      const int qbase = (qt_lo + s % per_head) * BN + 32 * hf;
+      const float4 *sp = a.stats + static_cast<size_t>(zq) * a.Lpad + qbase;
+      uint32_t gs[16], gt[16], pc[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const float4 st0 = __ldg(sp + e), st1 = __ldg(sp + e + 1);
+        const Grad2 g2 = grad_pair(sv[e], sv[e + 1], tv[e], tv[e + 1], uv[e], uv[e + 1],
+                                   krow > qbase + e, krow > qbase + e + 1, st0, st1, c, tau);
+        gs[e >> 1] = g2.gs;
+        gt[e >> 1] = g2.gt;
+        pc[e >> 1] = g2.pc;
+      }
+      if (s > 0) {
+        ok = mbar_wait(smem_u32(acc_done), (s - 1) & 1, ab);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const int cidx = 4 * hf + ch;
+        *reinterpret_cast<uint4 *>(prow + ((cidx ^ (row & 7)) << 4)) =
+            make_uint4(pc[4 * ch], pc[4 * ch + 1], pc[4 * ch + 2], pc[4 * ch + 3]);
+      }
+      tmem_st16(tl + COL_GS + 16 * hf, gs);
+      tmem_st16(tl + COL_GT + 16 * hf, gt);
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(gs_full));
+    }
+    if (ok) {
+      ok = mbar_wait(smem_u32(acc_full), 0, ab);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const bool valid = krow < a.L;
+        const size_t ro = (static_cast<size_t>(zk) * a.L + (valid ? krow : 0)) * D + 64 * hf;
+        store_acc_half(tl + COL_ACC0 + 64 * hf, a.g0 + ro, valid);
+        store_acc_half(tl + COL_ACC1 + 64 * hf, a.g1 + ro, valid);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace
+
+size_t prefill_bwd_stats_count(int B, int Hq, int L) {
+  const size_t lpad = (static_cast<size_t>(L) + STAT_ROWS - 1) / STAT_ROWS * STAT_ROWS;
+  return static_cast<size_t>(B) * Hq * lpad;
+}
+
+cudaError_t launch_prefill_bwd(const void *q, const void *k, const void *v, const void *r,
+                               const void *out, const void *o1, const float *lse,
+                               const float *sbar, const void *dout, void *dq, void *dk, void *dv,
+                               void *dr, int B, int Hq, int Hkv, int L, void *stats, unsigned *err,
+                               cudaStream_t stream) {
+  static thread_local int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         qk::SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kv::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return cudaErrorInvalidValue;
+  const int Lpad = (L + STAT_ROWS - 1) / STAT_ROWS * STAT_ROWS;
+  float4 *st = static_cast<float4 *>(stats);
+  const long long nrows = static_cast<long long>(B) * Hq * Lpad;
+  bwd_prep_kernel<<<static_cast<unsigned>((nrows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(o1),
+      static_cast<const __nv_bfloat16 *>(dout), lse, sbar, st, L, Lpad, nrows);
+
+  BwdArgs a;
+  a.stats = st;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.L = L;
+  a.Lpad = Lpad;
+  a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+  a.tau = 1.f / sqrtf(static_cast<float>(D));
+  a.err = err;
+
+  CUtensorMap mq, mr, mo, mk, mv;
+  // dQ / dR: 128-row query boxes, 64-row key boxes.
+  if (!make_head_rows_map(enc, &mq, q, L, B * Hq, qk::BM) ||
+      !make_head_rows_map(enc, &mr, r, L, B * Hq, qk::BM) ||
+      !make_head_rows_map(enc, &mo, dout, L, B * Hq, qk::BM) ||
+      !make_head_rows_map(enc, &mk, k, L, B * Hkv, qk::BN) ||
+      !make_head_rows_map(enc, &mv, v, L, B * Hkv, qk::BN))
+    return cudaErrorInvalidValue;
+  a.g0 = static_cast<__nv_bfloat16 *>(dq);
+  a.g1 = static_cast<__nv_bfloat16 *>(dr);
+  const int nq = (L + qk::BM - 1) / qk::BM * B * Hq;
+  bwd_dq_kernel<<<nq, THREADS, qk::SMEM_BYTES, stream>>>(mq, mr, mo, mk, mv, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  // dK / dV: 64-row query boxes, 128-row key boxes.
+  if (!make_head_rows_map(enc, &mq, q, L, B * Hq, kv::BN) ||
+      !make_head_rows_map(enc, &mr, r, L, B * Hq, kv::BN) ||
+      !make_head_rows_map(enc, &mo, dout, L, B * Hq, kv::BN) ||
+      !make_head_rows_map(enc, &mk, k, L, B * Hkv, kv::BM) ||
+      !make_head_rows_map(enc, &mv, v, L, B * Hkv, kv::BM))
+    return cudaErrorInvalidValue;
+  a.g0 = static_cast<__nv_bfloat16 *>(dv);
+  a.g1 = static_cast<__nv_bfloat16 *>(dk);
+  const int nk = (L + kv::BM - 1) / kv::BM * B * Hkv;
+  bwd_dkv_kernel<<<nk, THREADS, kv::SMEM_BYTES, stream>>>(mq, mr, mo, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace plx

@@ -82,6 +82,8 @@ struct PrefillArgs {
   __nv_bfloat16 *out;
   float *lse;
   float *cor;  // optional: |correction| / |o| per row
+  __nv_bfloat16 *o1;  // optional (training): o^SA = O1 / l per row, bf16
+  float *sbar;        // optional (training): sigma / l per row
   int Hq, Hkv, L, B, nqt, nitems;
   int Lk, qoff;  // keys per head; absolute position of query row 0 (Lk - L)
   float scale_log2;  // log2(e) / sqrt(d)
@@ -448,10 +450,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint4 *dst = reinterpret_cast<uint4 *>(orow + part * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          if (a.o1 != nullptr) {
+            // Saved for the backward pass: o^SA = O1 / l.
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o1[e] * inv, o1[e + 1] * inv);
+            uint4 *d1 = reinterpret_cast<uint4 *>(a.o1 + (static_cast<size_t>(it.zq) * a.L + grow) * D + part * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) d1[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
         }
       }
       if (a.lse != nullptr && grow < a.L)
         a.lse[static_cast<size_t>(it.zq) * a.L + grow] = (m_used + log2f(l)) * 0.6931471805599453f;
+      if (a.sbar != nullptr && grow < a.L) a.sbar[static_cast<size_t>(it.zq) * a.L + grow] = sg * inv;
       if (want_cor && grow < a.L)
         a.cor[static_cast<size_t>(it.zq) * a.L + grow] = osq > 0.f ? sqrtf(csq) / sqrtf(osq) : 0.f;
     }
@@ -465,7 +476,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, int L, int heads, int box_rows) {
+}  // namespace
+
+bool make_head_rows_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, int L, int heads,
+                        int box_rows) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
                               static_cast<cuuint64_t>(heads)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
@@ -477,11 +491,9 @@ bool make_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, int L, int h
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *r, void *out,
-                              float *lse, float *cor, int B, int Hq, int Hkv, int L, int Lk,
-                              unsigned *err, cudaStream_t stream) {
+                              float *lse, float *cor, void *o1, float *sbar, int B, int Hq, int Hkv,
+                              int L, int Lk, unsigned *err, cudaStream_t stream) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -494,13 +506,15 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorInvalidValue;
   CUtensorMap mq, mr, mk, mv;
-  if (!make_map(enc, &mq, q, L, B * Hq, BM) || !make_map(enc, &mr, r, L, B * Hq, BM) ||
-      !make_map(enc, &mk, k, Lk, B * Hkv, BN) || !make_map(enc, &mv, v, Lk, B * Hkv, BN))
+  if (!make_head_rows_map(enc, &mq, q, L, B * Hq, BM) || !make_head_rows_map(enc, &mr, r, L, B * Hq, BM) ||
+      !make_head_rows_map(enc, &mk, k, Lk, B * Hkv, BN) || !make_head_rows_map(enc, &mv, v, Lk, B * Hkv, BN))
     return cudaErrorInvalidValue;
   PrefillArgs a;
   a.out = static_cast<__nv_bfloat16 *>(out);
   a.lse = lse;
   a.cor = cor;
+  a.o1 = static_cast<__nv_bfloat16 *>(o1);
+  a.sbar = sbar;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.L = L;

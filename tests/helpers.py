@@ -78,3 +78,22 @@ def assert_cor_close(got, ref, what=""):
     assert not got.size or excess.flat[worst] <= 0, (
         f"{what}: cor {got.flat[worst]:.5f} vs {ref.flat[worst]:.5f}")
     return float(np.max(np.abs(got - ref))) if got.size else 0.0
+
+
+# Gradients from the bf16 backward: the kernels round w c, tau ds and dt to
+# bf16 before the gradient GEMMs (2^-9 relative per term), read o and o^SA as
+# bf16, and round the result to bf16; the relative factor allows 5x those
+# roundings against the largest gradient of the tensor.
+GRAD_REL = 1e-2
+
+
+def assert_grad_close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite gradient"
+    err = np.max(np.abs(got - ref))
+    scale = np.max(np.abs(ref))
+    print(f"{what}: max|err| / max|ref| = {err / scale:.3e}")
+    assert err <= GRAD_REL * scale, f"{what}: max|err| {err:.3e} > {GRAD_REL} * {scale:.3e}"
+    return err / scale
