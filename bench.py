@@ -396,6 +396,19 @@ def main():
         td = launch_s(lambda: plx_decode_fwd_cor(dq, dr, kc, vc, sl, dout, dcor), 10)
         extra[wd.name + "_with_cor"] = {"value": dbytes / td / 1e9, "unit": "GB/s", "ms": td * 1e3,
                                         "frac_of_peak": dbytes / td / 1e9 / hbm_peak}
+        # Training: the forward that saves o^SA and sbar, and the backward
+        # (algorithmic flops: 8 length-d dot products per causal pair, twice
+        # the forward's).
+        from parametrized_local_linear_gb300 import plx_prefill_bwd, plx_prefill_fwd_train
+        o_t, lse_t, o1_t, sb_t = plx_prefill_fwd_train(q, k, v, r)
+        do_t = torch.randn(q.shape, device=dev, dtype=torch.float32).to(q.dtype)
+        gq, gk, gv, gr = (torch.empty_like(x) for x in (q, k, v, r))
+        tflops(wp.name + "_forward_train", wp.flops,
+               launch_s(lambda: plx_prefill_fwd_train(q, k, v, r, o_t, lse_t, o1_t, sb_t), 10))
+        tflops(wp.name + "_backward", 2 * wp.flops,
+               launch_s(lambda: plx_prefill_bwd(q, k, v, r, o_t, o1_t, lse_t, sb_t, do_t,
+                                                gq, gk, gv, gr), 10))
+        del o_t, lse_t, o1_t, sb_t, do_t, gq, gk, gv, gr
         w5 = inputs.DECODE_RAGGED
         d5 = inputs.decode_inputs_for(w5, device=dev)
         sl5 = d5[4].to(dev)

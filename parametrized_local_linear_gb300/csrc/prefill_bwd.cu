@@ -15,7 +15,9 @@
 //   dk_j   += tau ds_j q + dt_j rho
 // (the tests check this form against autograd through the explicit
 // covariance). The forward saves lse, o^SA and sbar per row; a small kernel
-// turns them into one record per row {lse log2 e, 1 + sbar, a, D}.
+// turns them into a record per row, {-lse log2 e, 1 + sbar, a, -D}, stored
+// interleaved by pairs of rows ({x0, x1, y0, y1, ...}, 32 bytes per pair) so
+// that two adjacent queries' records load as packed fp32x2 operands.
 //
 // Two kernels then stream the causal pairs, each with the same TMEM plan
 // (512 columns): S [0,64) T [64,128) U [128,192) packed bf16 score and probe
@@ -29,11 +31,16 @@
 // Neither kernel needs atomics: each output row is owned by one CTA. The
 // elementwise warps release S, T and U as soon as they have loaded them
 // (stu_free), so the next tile's score UMMAs run under the elementwise work
-// and the current tile's gradient UMMAs. 10 warps: 0 TMA producer, 1 TMEM
-// allocator + UMMA issuer, 2..9 elementwise (two warps per TMEM lane quarter,
-// each taking half of the tile's 64 columns; there is no row reduction, so
-// the columns split freely).
+// and the current tile's gradient UMMAs. 12 warps: 0 TMA producer; 1, 2, 3
+// one UMMA-issuing thread each (warp 1 also allocates TMEM); 4..11
+// elementwise (two warps per TMEM lane quarter, each taking half of the
+// tile's 64 columns; there is no row reduction, so the columns split
+// freely). The UMMAs are spread over three threads because one thread
+// cannot issue tcgen05.mma as fast as the tensor core retires these shapes
+// (measured 50-100 cycles per issue under load against 48-64 cycles of work).
 #include <math.h>
+
+#include <type_traits>
 
 #include "plx_device.cuh"
 #include "plx_internal.h"
@@ -42,7 +49,8 @@ namespace plx {
 namespace {
 
 constexpr int D = 128;
-constexpr int THREADS = 32 * 10;
+constexpr int THREADS = 32 * 12;
+constexpr int EW_WARP0 = 4;               // first elementwise warp
 constexpr int NEW = 256;                  // elementwise threads
 constexpr uint32_t COL_S = 0, COL_T = 64, COL_U = 128, COL_GS = 192, COL_GT = 224;
 constexpr uint32_t COL_ACC0 = 256, COL_ACC1 = 384;
@@ -50,7 +58,7 @@ constexpr int STAT_ROWS = 64;             // stats rows are padded to this multi
 
 struct BwdArgs {
   __nv_bfloat16 *g0, *g1;  // dq, dr (dq kernel) or dv, dk (dkv kernel)
-  const float4 *stats;     // [B * Hq][Lpad] {lse log2 e, 1 + sbar, a, D}
+  const float *stats;      // [B * Hq][Lpad / 2][8] row-pair records (see above)
   int B, Hq, Hkv, L, Lpad;
   float scale_log2, tau;
   unsigned *err;
@@ -61,15 +69,21 @@ struct BwdArgs {
 __global__ void __launch_bounds__(256) bwd_prep_kernel(
     const __nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *__restrict__ o1,
     const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ lse,
-    const float *__restrict__ sbar, float4 *__restrict__ stats, int L, int Lpad, long long nrows) {
+    const float *__restrict__ sbar, float *__restrict__ stats, int L, int Lpad, long long nrows) {
   const long long p = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= nrows) return;
   const long long zh = p / Lpad;
   const int i = static_cast<int>(p - zh * Lpad);
+  float *rec = stats + (p >> 1) * 8 + (p & 1);  // Lpad is even: pairs stay within a head
   if (i >= L) {
     // Padding rows: weight 2^-inf = 0 for every key.
-    if (lane == 0) stats[p] = make_float4(INFINITY, 1.f, 0.f, 0.f);
+    if (lane == 0) {
+      rec[0] = -INFINITY;
+      rec[2] = 1.f;
+      rec[4] = 0.f;
+      rec[6] = 0.f;
+    }
     return;
   }
   const long long row = zh * L + i;
@@ -92,30 +106,43 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(
   }
   if (lane == 0) {
     const float sb = sbar[row];
-    stats[p] = make_float4(lse[row] * 1.4426950408889634f, 1.f + sb, ga, fmaf(ga, sb, go));
+    rec[0] = -lse[row] * 1.4426950408889634f;
+    rec[2] = 1.f + sb;
+    rec[4] = ga;
+    rec[6] = -fmaf(ga, sb, go);
   }
 }
 
-// Gradients of two columns of one (query, key) row pair block: inputs raw
-// scores s, probe products t, u = g . v; outputs tau * ds, dt and w c.
+// Gradients of two adjacent (query, key) pairs in packed fp32x2 arithmetic.
+// Inputs: raw scores s, probe products t, u = g . v for the two pairs, and
+// per pair the record {lse log2 e, 1 + sbar, a, D} split into packed
+// components (for the query-block kernel both pairs share one query, for the
+// key-block kernel they are two queries). Outputs: tau ds and dt (and w c
+// when PC) as packed bf16. MASK: the pair block reaches the causal diagonal
+// and m0 / m1 drop the pairs whose key lies after the query.
+struct Stat2 {
+  uint64_t nlse, s1, a, nd;  // -lse log2 e, 1 + sbar, a, -D
+};
 struct Grad2 {
   uint32_t gs, gt, pc;
 };
-__device__ __forceinline__ Grad2 grad_pair(float s0, float s1, float t0, float t1, float u0, float u1,
-                                           bool m0, bool m1, float4 st0, float4 st1, float c,
-                                           float tau) {
-  // st = {lse log2 e, 1 + sbar, a, D}
-  float w0 = fast_exp2(fmaf(s0, c, -st0.x));
-  float w1 = fast_exp2(fmaf(s1, c, -st1.x));
-  w0 = m0 ? 0.f : w0;
-  w1 = m1 ? 0.f : w1;
-  const float c0 = st0.y - t0, c1 = st1.y - t1;
-  const float d0 = fmaf(c0, u0, fmaf(st0.z, t0, -st0.w));
-  const float d1 = fmaf(c1, u1, fmaf(st1.z, t1, -st1.w));
+template <bool MASK, bool PC>
+__device__ __forceinline__ Grad2 grad_pair(uint64_t s, uint64_t t, uint64_t u, const Stat2 &st,
+                                           bool m0, bool m1, uint64_t c2, uint64_t tau2) {
+  const uint64_t neg1 = f2(-1.f, -1.f);
+  const uint64_t x = ffma2(s, c2, st.nlse);
+  float w0 = fast_exp2(f2lo(x)), w1 = fast_exp2(f2hi(x));
+  if (MASK) {
+    w0 = m0 ? 0.f : w0;
+    w1 = m1 ? 0.f : w1;
+  }
+  const uint64_t w = f2(w0, w1);
+  const uint64_t cc = ffma2(t, neg1, st.s1);                // 1 + sbar - t
+  const uint64_t dd = ffma2(cc, u, ffma2(st.a, t, st.nd));  // c u + a t - D
   Grad2 r;
-  r.gs = pack_bf16x2(w0 * d0 * tau, w1 * d1 * tau);
-  r.gt = pack_bf16x2(w0 * (st0.z - u0), w1 * (st1.z - u1));
-  r.pc = pack_bf16x2(w0 * c0, w1 * c1);
+  r.gs = pack_bf16x2(fmul2(fmul2(w, tau2), dd));
+  r.gt = pack_bf16x2(fmul2(w, ffma2(u, neg1, st.a)));       // w (a - u)
+  if (PC) r.pc = pack_bf16x2(fmul2(w, cc));
   return r;
 }
 
@@ -150,7 +177,7 @@ constexpr int OFF_Q = 0, OFF_R = 2 * HALF_Q, OFF_DO = 4 * HALF_Q;
 constexpr int OFF_K = 6 * HALF_Q;              // 98304
 constexpr int OFF_V = OFF_K + NST * TILE_KV;   // 147456
 constexpr int OFF_BAR = OFF_V + NST * TILE_KV; // 196608
-constexpr int NBAR = 1 + 4 * NST + 6;
+constexpr int NBAR = 1 + 4 * NST + 5 + 3;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
 }  // namespace qk
 
@@ -165,15 +192,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *q_full = bars;              // Q, R, dO loaded
   uint64_t *k_full = bars + 1;
-  uint64_t *k_empty = k_full + NST;     // dQ / dR UMMAs of the tile done
-  uint64_t *v_full = k_empty + NST;
-  uint64_t *v_empty = v_full + NST;     // U UMMAs of the tile done
-  uint64_t *stu_full = v_empty + NST;   // S, T, U of the tile in TMEM
+  uint64_t *k_empty = k_full + NST;     // count 2: dQ and dR UMMAs of the tile done
+  uint64_t *v_empty = k_empty + NST;    // U UMMAs of the tile done
+  uint64_t *v_full = v_empty + NST;
+  uint64_t *stu_full = v_full + NST;    // count 3: S, T, U of the tile in TMEM
   uint64_t *stu_free = stu_full + 1;    // count 256: S, T, U loaded by every thread
   uint64_t *gs_full = stu_free + 1;     // count 256: dS, dT written
-  uint64_t *acc_done = gs_full + 1;     // dQ / dR UMMAs of the tile done
-  uint64_t *acc_full = acc_done + 1;    // every UMMA done (epilogue)
-  uint64_t *drain = acc_full + 1;
+  uint64_t *acc_done = gs_full + 1;     // count 2: dQ and dR UMMAs of the tile done
+  uint64_t *acc_full = acc_done + 1;    // count 2: every gradient UMMA done (epilogue)
+  uint64_t *drain = acc_full + 1;       // [3] one per issuing thread
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -190,16 +217,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(smem_u32(q_full), 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
-      mbar_init(smem_u32(&k_empty[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 2);
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
-    mbar_init(smem_u32(stu_full), 1);
+    mbar_init(smem_u32(stu_full), 3);
     mbar_init(smem_u32(stu_free), NEW);
     mbar_init(smem_u32(gs_full), NEW);
-    mbar_init(smem_u32(acc_done), 1);
-    mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(acc_done), 2);
+    mbar_init(smem_u32(acc_full), 2);
+    for (int x = 0; x < 3; ++x) mbar_init(smem_u32(&drain[x]), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -257,67 +284,73 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait_drain(smem_u32(&v_full[j % NST]), (j / NST) & 1);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp < EW_WARP0) {
     if (lane == 0) {
-      // ---------------------------------------------------------- UMMA issuer
+      // ---------------------------------------------------------- UMMA issuers
+      // role 0: S = Q K^T and dQ += dS K; role 1: T = R K^T and dR += dT K;
+      // role 2: U = dO V^T. K-major operands for the scores, K MN-major for
+      // the gradients.
+      const int role = warp - 1;
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, 1);
-      const uint64_t qdesc = smem_desc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
-      const uint64_t rdesc = smem_desc_sw128(smem_u32(smem + OFF_R), 16, 1024);
-      const uint64_t odesc = smem_desc_sw128(smem_u32(smem + OFF_DO), 16, 1024);
-      const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
-      const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + OFF_V), 16, 1024);
+      const uint64_t adesc =
+          smem_desc_sw128(smem_u32(smem + (role == 0 ? OFF_Q : role == 1 ? OFF_R : OFF_DO)), 16, 1024);
+      const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + (role == 2 ? OFF_V : OFF_K)), 16, 1024);
       const uint64_t kmn0 = smem_desc_sw128(smem_u32(smem + OFF_K), HALF_KV, 1024);
+      const uint32_t dcol = tbase + (role == 0 ? COL_S : role == 1 ? COL_T : COL_U);
+      const uint32_t gcol = tbase + (role == 0 ? COL_GS : COL_GT);
+      const uint32_t acol = tbase + (role == 0 ? COL_ACC0 : COL_ACC1);
+      uint64_t *b_full = role == 2 ? v_full : k_full;
       bool ok = mbar_wait(smem_u32(q_full), 0, ab);
-      // S, T, U of tile j (K-major operands on both sides).
-      auto issue_stu = [&](int j) -> bool {
-        const int st = j % NST, ph = (j / NST) & 1;
-        if (!mbar_wait(smem_u32(&k_full[st]), ph, ab)) return false;
-        if (!mbar_wait(smem_u32(&v_full[st]), ph, ab)) return false;
+      auto issue_score = [&](int j) -> bool {
+        const int st = j % NST;
+        if (!mbar_wait(smem_u32(&b_full[st]), (j / NST) & 1, ab)) return false;
         tc_fence_after();
-        const uint64_t kd = kdesc0 + st * (TILE_KV >> 4), vd = vdesc0 + st * (TILE_KV >> 4);
+        const uint64_t bd = bdesc0 + st * (TILE_KV >> 4);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ao = (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2;
-          const uint32_t bo = (ks >> 2) * (HALF_KV >> 4) + (ks & 3) * 2;
-          umma_ss(tbase + COL_S, qdesc + ao, kd + bo, idesc_s, ks > 0);
-          umma_ss(tbase + COL_T, rdesc + ao, kd + bo, idesc_s, ks > 0);
-          umma_ss(tbase + COL_U, odesc + ao, vd + bo, idesc_s, ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(dcol, adesc + (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2,
+                  bd + (ks >> 2) * (HALF_KV >> 4) + (ks & 3) * 2, idesc_s, ks > 0);
         umma_commit(smem_u32(stu_full));
-        umma_commit(smem_u32(&v_empty[st]));
+        if (role == 2) umma_commit(smem_u32(&v_empty[st]));
         return true;
       };
-      ok = ok && issue_stu(0);
+      ok = ok && issue_score(0);
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n) {
           // S, T, U of tile j are in registers once stu_free completes.
-          if (!mbar_wait(smem_u32(stu_free), j & 1, ab) || !issue_stu(j + 1)) break;
+          if (!mbar_wait(smem_u32(stu_free), j & 1, ab) || !issue_score(j + 1)) break;
         }
+        if (role == 2) continue;
         if (!mbar_wait(smem_u32(gs_full), j & 1, ab)) break;
         tc_fence_after();
         const int st = j % NST;
         const uint64_t km = kmn0 + st * (TILE_KV >> 4);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          umma_ts(tbase + COL_ACC0, tbase + COL_GS + ks * 8, km + ks * (2048 >> 4), idesc_g, (j > 0 || ks > 0));
-          umma_ts(tbase + COL_ACC1, tbase + COL_GT + ks * 8, km + ks * (2048 >> 4), idesc_g, (j > 0 || ks > 0));
-        }
+        for (int ks = 0; ks < BN / 16; ++ks)
+          umma_ts(acol, gcol + ks * 8, km + ks * (2048 >> 4), idesc_g, (j > 0 || ks > 0));
         umma_commit(smem_u32(acc_done));
         umma_commit(smem_u32(&k_empty[st]));
       }
-      umma_commit(smem_u32(acc_full));
-      umma_commit(smem_u32(drain));
-      mbar_wait_drain(smem_u32(drain), 0);
+      if (role != 2) umma_commit(smem_u32(acc_full));
+      umma_commit(smem_u32(&drain[role]));
+      mbar_wait_drain(smem_u32(&drain[role]), 0);
     }
   } else {
     // ------------------------------------------------------------ elementwise
-    const int qw = warp & 3, hf = (warp - 2) >> 2;
+    const int qw = warp & 3, hf = (warp - EW_WARP0) >> 2;
     const int row = qw * 32 + lane, grow = q0 + row;
     const uint32_t tl = tbase + (static_cast<uint32_t>(qw * 32) << 16);
-    const float4 st = grow < a.L ? a.stats[static_cast<size_t>(zq) * a.Lpad + grow]
-                                 : make_float4(INFINITY, 1.f, 0.f, 0.f);
-    const float c = a.scale_log2, tau = a.tau;
+    float nl = -INFINITY, s1 = 1.f, aa = 0.f, nd = 0.f;
+    if (grow < a.L) {
+      const float *rec = a.stats + ((static_cast<size_t>(zq) * a.Lpad + grow) >> 1) * 8 + (grow & 1);
+      nl = rec[0];
+      s1 = rec[2];
+      aa = rec[4];
+      nd = rec[6];
+    }
+    const Stat2 st2{f2(nl, nl), f2(s1, s1), f2(aa, aa), f2(nd, nd)};
+    const uint64_t c2 = f2(a.scale_log2, a.scale_log2), tau2 = f2(a.tau, a.tau);
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       ok = mbar_wait(smem_u32(stu_full), j & 1, ab);
@@ -332,12 +365,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_arrive(smem_u32(stu_free));
       const int kbase = j * BN + 32 * hf;
       uint32_t gs[16], gt[16];
+      if (j * BN + BN - 1 > q0) {  // the tile reaches the diagonal
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const Grad2 g2 = grad_pair(s[e], s[e + 1], t[e], t[e + 1], u[e], u[e + 1], kbase + e > grow,
-                                   kbase + e + 1 > grow, st, st, c, tau);
-        gs[e >> 1] = g2.gs;
-        gt[e >> 1] = g2.gt;
+        for (int e = 0; e < 32; e += 2) {
+          const Grad2 g2 = grad_pair<true, false>(f2(s[e], s[e + 1]), f2(t[e], t[e + 1]),
+                                                  f2(u[e], u[e + 1]), st2, kbase + e > grow,
+                                                  kbase + e + 1 > grow, c2, tau2);
+          gs[e >> 1] = g2.gs;
+          gt[e >> 1] = g2.gt;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const Grad2 g2 = grad_pair<false, false>(f2(s[e], s[e + 1]), f2(t[e], t[e + 1]),
+                                                   f2(u[e], u[e + 1]), st2, false, false, c2, tau2);
+          gs[e >> 1] = g2.gs;
+          gt[e >> 1] = g2.gt;
+        }
       }
       if (j > 0) {
         // The previous tile's dQ / dR UMMAs read the gradient columns.
@@ -384,7 +428,7 @@ constexpr int OFF_K = 0, OFF_V = 2 * HALF_K;
 constexpr int OFF_P = 4 * HALF_K;              // 65536: (w c)^T tile, 128 keys x 64 queries bf16
 constexpr int OFF_STG = OFF_P + BM * BN * 2;   // 81920
 constexpr int OFF_BAR = OFF_STG + NST * STAGE; // 229376
-constexpr int NBAR = 1 + 2 * NST + 6;
+constexpr int NBAR = 1 + 2 * NST + 5 + 3;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
 }  // namespace kv
 
@@ -399,13 +443,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *kv_full = bars;             // K and V blocks loaded
   uint64_t *q_full = bars + 1;          // [NST] Q, R, dO of a step loaded
-  uint64_t *q_empty = q_full + NST;     // [NST] the step's dV / dK UMMAs done
-  uint64_t *stu_full = q_empty + NST;
+  uint64_t *q_empty = q_full + NST;     // [NST] count 2: the step's dV and dK UMMAs done
+  uint64_t *stu_full = q_empty + NST;   // count 3
   uint64_t *stu_free = stu_full + 1;    // count 256
   uint64_t *gs_full = stu_free + 1;     // count 256: (w c)^T in smem, dS^T / dT^T in TMEM
-  uint64_t *acc_done = gs_full + 1;
-  uint64_t *acc_full = acc_done + 1;
-  uint64_t *drain = acc_full + 1;
+  uint64_t *acc_done = gs_full + 1;     // count 2
+  uint64_t *acc_full = acc_done + 1;    // count 2
+  uint64_t *drain = acc_full + 1;       // [3]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -424,14 +468,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(smem_u32(kv_full), 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&q_full[s]), 1);
-      mbar_init(smem_u32(&q_empty[s]), 1);
+      mbar_init(smem_u32(&q_empty[s]), 2);
     }
-    mbar_init(smem_u32(stu_full), 1);
+    mbar_init(smem_u32(stu_full), 3);
     mbar_init(smem_u32(stu_free), NEW);
     mbar_init(smem_u32(gs_full), NEW);
-    mbar_init(smem_u32(acc_done), 1);
-    mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(acc_done), 2);
+    mbar_init(smem_u32(acc_full), 2);
+    for (int x = 0; x < 3; ++x) mbar_init(smem_u32(&drain[x]), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -483,69 +527,83 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait_drain(smem_u32(&q_full[s % NST]), (s / NST) & 1);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp < EW_WARP0) {
     if (lane == 0) {
-      // ---------------------------------------------------------- UMMA issuer
+      // ---------------------------------------------------------- UMMA issuers
+      // role 0: S^T = K Q^T and dV += (w c)^T dO; role 1: T^T = K R^T and
+      // dK += (tau dS)^T Q + dT^T R (one thread, so the accumulator's first
+      // write comes first); role 2: U^T = V dO^T.
+      const int role = warp - 1;
       constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, 1);
-      const uint64_t kdesc = smem_desc_sw128(smem_u32(smem + OFF_K), 16, 1024);
-      const uint64_t vdesc = smem_desc_sw128(smem_u32(smem + OFF_V), 16, 1024);
+      const uint64_t adesc = smem_desc_sw128(smem_u32(smem + (role == 2 ? OFF_V : OFF_K)), 16, 1024);
       const uint64_t pdesc = smem_desc_sw128(smem_u32(smem + OFF_P), 16, 1024);
-      const uint64_t stg_k = smem_desc_sw128(smem_u32(smem + OFF_STG), 16, 1024);        // K-major view
-      const uint64_t stg_mn = smem_desc_sw128(smem_u32(smem + OFF_STG), HALF_Q, 1024);   // MN-major view
+      // Stage operand `role` (Q, R, dO) in its K-major and MN-major views.
+      const uint64_t stg_k = smem_desc_sw128(smem_u32(smem + OFF_STG + role * TILE_Q), 16, 1024);
+      const uint64_t stg_mn = smem_desc_sw128(smem_u32(smem + OFF_STG), HALF_Q, 1024);
+      const uint32_t dcol = tbase + (role == 0 ? COL_S : role == 1 ? COL_T : COL_U);
       bool ok = mbar_wait(smem_u32(kv_full), 0, ab);
-      auto issue_stu = [&](int s) -> bool {
+      auto issue_score = [&](int s) -> bool {
         const int st = s % NST;
         if (!mbar_wait(smem_u32(&q_full[st]), (s / NST) & 1, ab)) return false;
         tc_fence_after();
-        const uint64_t qd = stg_k + st * (STAGE >> 4);
-        const uint64_t rd = qd + (TILE_Q >> 4), od = qd + 2 * (TILE_Q >> 4);
+        const uint64_t bd = stg_k + st * (STAGE >> 4);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t ao = (ks >> 2) * (HALF_K >> 4) + (ks & 3) * 2;
-          const uint32_t bo = (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2;
-          umma_ss(tbase + COL_S, kdesc + ao, qd + bo, idesc_s, ks > 0);
-          umma_ss(tbase + COL_T, kdesc + ao, rd + bo, idesc_s, ks > 0);
-          umma_ss(tbase + COL_U, vdesc + ao, od + bo, idesc_s, ks > 0);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(dcol, adesc + (ks >> 2) * (HALF_K >> 4) + (ks & 3) * 2,
+                  bd + (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2, idesc_s, ks > 0);
         umma_commit(smem_u32(stu_full));
         return true;
       };
-      ok = ok && issue_stu(0);
+      ok = ok && issue_score(0);
       for (int s = 0; ok && s < n; ++s) {
         if (s + 1 < n) {
-          if (!mbar_wait(smem_u32(stu_free), s & 1, ab) || !issue_stu(s + 1)) break;
+          if (!mbar_wait(smem_u32(stu_free), s & 1, ab) || !issue_score(s + 1)) break;
         }
+        if (role == 2) continue;
         if (!mbar_wait(smem_u32(gs_full), s & 1, ab)) break;
         tc_fence_after();
         const int st = s % NST;
         const uint64_t qm = stg_mn + st * (STAGE >> 4);
         const uint64_t rm = qm + (TILE_Q >> 4), om = qm + 2 * (TILE_Q >> 4);
+        if (role == 0) {
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          // dV += (w c)^T dO;  dK += (tau dS)^T Q + dT^T R.
-          umma_ss(tbase + COL_ACC0, pdesc + ks * 2, om + ks * (2048 >> 4), idesc_g, (s > 0 || ks > 0));
-          umma_ts(tbase + COL_ACC1, tbase + COL_GS + ks * 8, qm + ks * (2048 >> 4), idesc_g, (s > 0 || ks > 0));
-          umma_ts(tbase + COL_ACC1, tbase + COL_GT + ks * 8, rm + ks * (2048 >> 4), idesc_g, 1);
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ss(tbase + COL_ACC0, pdesc + ks * 2, om + ks * (2048 >> 4), idesc_g, (s > 0 || ks > 0));
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ts(tbase + COL_ACC1, tbase + COL_GS + ks * 8, qm + ks * (2048 >> 4), idesc_g, (s > 0 || ks > 0));
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ts(tbase + COL_ACC1, tbase + COL_GT + ks * 8, rm + ks * (2048 >> 4), idesc_g, 1);
         }
         umma_commit(smem_u32(acc_done));
         umma_commit(smem_u32(&q_empty[st]));
       }
-      umma_commit(smem_u32(acc_full));
-      umma_commit(smem_u32(drain));
-      mbar_wait_drain(smem_u32(drain), 0);
+      if (role != 2) umma_commit(smem_u32(acc_full));
+      umma_commit(smem_u32(&drain[role]));
+      mbar_wait_drain(smem_u32(&drain[role]), 0);
     }
   } else {
     // ------------------------------------------------------------ elementwise
-    const int qw = warp & 3, hf = (warp - 2) >> 2;
+    const int qw = warp & 3, hf = (warp - EW_WARP0) >> 2;
     const int row = qw * 32 + lane, krow = k0 + row;
     const uint32_t tl = tbase + (static_cast<uint32_t>(qw * 32) << 16);
     // This thread's row of the (w c)^T tile: 128-byte rows, 16-byte chunks
     // XOR-swizzled by the row index within each 8-row group (SW128, K-major).
     uint8_t *prow = smem + OFF_P + (row >> 3) * 1024 + (row & 7) * 128;
-    const float c = a.scale_log2, tau = a.tau;
+    const uint64_t c2 = f2(a.scale_log2, a.scale_log2), tau2 = f2(a.tau, a.tau);
     bool ok = true;
     for (int s = 0; s < n; ++s) {
+      const int zq = b * a.Hq + kvh * G + s / per_head;
+      const int qbase = (qt_lo + s % per_head) * BN + 32 * hf;
+      // The records of this half's 32 queries are 16 pairs x 32 bytes: lane l
+      // loads 16 of them (pair l / 2, half l & 1), before the TMEM wait so the
+      // load overlaps it, and the pairs are handed round by warp shuffles
+      // (per-column loads from every lane stalled on their latency).
+      const float4 mine = __ldg(reinterpret_cast<const float4 *>(
+                                    a.stats + (static_cast<size_t>(zq) * a.Lpad + qbase) * 4) + lane);
       ok = mbar_wait(smem_u32(stu_full), s & 1, ab);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -556,19 +614,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(smem_u32(stu_free));
-      const int zq = b * a.Hq + kvh * G + s / per_head;
-      const int qbase = (qt_lo + s % per_head) * BN + 32 * hf;
-      const float4 *sp = a.stats + static_cast<size_t>(zq) * a.Lpad + qbase;
       uint32_t gs[16], gt[16], pc[16];
+      auto cols = [&](auto mask_tag) {
+        constexpr bool M = decltype(mask_tag)::value;
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float4 st0 = __ldg(sp + e), st1 = __ldg(sp + e + 1);
-        const Grad2 g2 = grad_pair(sv[e], sv[e + 1], tv[e], tv[e + 1], uv[e], uv[e + 1],
-                                   krow > qbase + e, krow > qbase + e + 1, st0, st1, c, tau);
-        gs[e >> 1] = g2.gs;
-        gt[e >> 1] = g2.gt;
-        pc[e >> 1] = g2.pc;
-      }
+        for (int e = 0; e < 32; e += 2) {
+          // Pair (qbase + e, qbase + e + 1): lanes e and e + 1 hold it.
+          const Stat2 st2{f2(__shfl_sync(0xffffffffu, mine.x, e), __shfl_sync(0xffffffffu, mine.y, e)),
+                          f2(__shfl_sync(0xffffffffu, mine.z, e), __shfl_sync(0xffffffffu, mine.w, e)),
+                          f2(__shfl_sync(0xffffffffu, mine.x, e + 1), __shfl_sync(0xffffffffu, mine.y, e + 1)),
+                          f2(__shfl_sync(0xffffffffu, mine.z, e + 1), __shfl_sync(0xffffffffu, mine.w, e + 1))};
+          const Grad2 g2 = grad_pair<M, true>(f2(sv[e], sv[e + 1]), f2(tv[e], tv[e + 1]),
+                                              f2(uv[e], uv[e + 1]), st2, krow > qbase + e,
+                                              krow > qbase + e + 1, c2, tau2);
+          gs[e >> 1] = g2.gs;
+          gt[e >> 1] = g2.gt;
+          pc[e >> 1] = g2.pc;
+        }
+      };
+      // Mask only where the block reaches the causal diagonal.
+      if (k0 + BM - 1 > (qt_lo + s % per_head) * BN) cols(std::true_type{});
+      else cols(std::false_type{});
       if (s > 0) {
         ok = mbar_wait(smem_u32(acc_done), (s - 1) & 1, ab);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -634,7 +700,7 @@ cudaError_t launch_prefill_bwd(const void *q, const void *k, const void *v, cons
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorInvalidValue;
   const int Lpad = (L + STAT_ROWS - 1) / STAT_ROWS * STAT_ROWS;
-  float4 *st = static_cast<float4 *>(stats);
+  float *st = static_cast<float *>(stats);
   const long long nrows = static_cast<long long>(B) * Hq * Lpad;
   bwd_prep_kernel<<<static_cast<unsigned>((nrows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(o1),
