@@ -65,51 +65,58 @@ struct BwdArgs {
 };
 
 // ---------------------------------------------------------------- per-row records
-// One warp per (padded) row: a = g . o^SA, D = g . o + a sbar.
+// Half a warp per (padded) row, 16 bytes of each tensor per lane:
+// a = g . o^SA, D = g . o + a sbar.
+__device__ __forceinline__ float dot8(uint4 x, uint4 y) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xs[i]));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ys[i]));
+    acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+  }
+  return acc;
+}
+
 __global__ void __launch_bounds__(256) bwd_prep_kernel(
     const __nv_bfloat16 *__restrict__ out, const __nv_bfloat16 *__restrict__ o1,
     const __nv_bfloat16 *__restrict__ dout, const float *__restrict__ lse,
     const float *__restrict__ sbar, float *__restrict__ stats, int L, int Lpad, long long nrows) {
-  const long long p = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (p >= nrows) return;
+  const long long p = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
+  const int sub = threadIdx.x & 15;
+  if (p >= nrows) return;  // uniform per half warp; nrows is even, so whole warps exit together
   const long long zh = p / Lpad;
   const int i = static_cast<int>(p - zh * Lpad);
   float *rec = stats + (p >> 1) * 8 + (p & 1);  // Lpad is even: pairs stay within a head
-  if (i >= L) {
-    // Padding rows: weight 2^-inf = 0 for every key.
-    if (lane == 0) {
+  float go = 0.f, ga = 0.f;
+  const bool valid = i < L;
+  const long long row = zh * L + i;
+  if (valid) {
+    const size_t off = static_cast<size_t>(row) * D + sub * 8;
+    const uint4 gv = *reinterpret_cast<const uint4 *>(dout + off);
+    go = dot8(gv, *reinterpret_cast<const uint4 *>(out + off));
+    ga = dot8(gv, *reinterpret_cast<const uint4 *>(o1 + off));
+  }
+#pragma unroll
+  for (int sh = 8; sh > 0; sh >>= 1) {
+    go += __shfl_xor_sync(0xffffffffu, go, sh);
+    ga += __shfl_xor_sync(0xffffffffu, ga, sh);
+  }
+  if (sub == 0) {
+    if (valid) {
+      const float sb = sbar[row];
+      rec[0] = -lse[row] * 1.4426950408889634f;
+      rec[2] = 1.f + sb;
+      rec[4] = ga;
+      rec[6] = -fmaf(ga, sb, go);
+    } else {
+      // Padding rows: weight 2^-inf = 0 for every key.
       rec[0] = -INFINITY;
       rec[2] = 1.f;
       rec[4] = 0.f;
       rec[6] = 0.f;
     }
-    return;
-  }
-  const long long row = zh * L + i;
-  const size_t off = static_cast<size_t>(row) * D + lane * 4;
-  const uint2 gv = *reinterpret_cast<const uint2 *>(dout + off);
-  const uint2 ov = *reinterpret_cast<const uint2 *>(out + off);
-  const uint2 av = *reinterpret_cast<const uint2 *>(o1 + off);
-  const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gv.x));
-  const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&gv.y));
-  const float2 o0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ov.x));
-  const float2 o1v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ov.y));
-  const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&av.x));
-  const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&av.y));
-  float go = g0.x * o0.x + g0.y * o0.y + g1.x * o1v.x + g1.y * o1v.y;
-  float ga = g0.x * a0.x + g0.y * a0.y + g1.x * a1.x + g1.y * a1.y;
-#pragma unroll
-  for (int sh = 16; sh > 0; sh >>= 1) {
-    go += __shfl_xor_sync(0xffffffffu, go, sh);
-    ga += __shfl_xor_sync(0xffffffffu, ga, sh);
-  }
-  if (lane == 0) {
-    const float sb = sbar[row];
-    rec[0] = -lse[row] * 1.4426950408889634f;
-    rec[2] = 1.f + sb;
-    rec[4] = ga;
-    rec[6] = -fmaf(ga, sb, go);
   }
 }
 
@@ -702,7 +709,7 @@ cudaError_t launch_prefill_bwd(const void *q, const void *k, const void *v, cons
   const int Lpad = (L + STAT_ROWS - 1) / STAT_ROWS * STAT_ROWS;
   float *st = static_cast<float *>(stats);
   const long long nrows = static_cast<long long>(B) * Hq * Lpad;
-  bwd_prep_kernel<<<static_cast<unsigned>((nrows + 7) / 8), 256, 0, stream>>>(
+  bwd_prep_kernel<<<static_cast<unsigned>((nrows + 15) / 16), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(o1),
       static_cast<const __nv_bfloat16 *>(dout), lse, sbar, st, L, Lpad, nrows);
 
