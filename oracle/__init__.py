@@ -220,3 +220,25 @@ def _parallel(fn, items, threads):
     # threads give real parallelism here (and are safe next to CUDA).
     with ThreadPoolExecutor(max_workers=min(threads, len(items))) as ex:
         list(ex.map(fn, items))
+
+
+def qkvr_projection(x, w, B, L, Hq, Hkv, d):
+    """The four input projections of a Parallax layer in one product.
+
+    Page "Parallax: parametrized local linear attention for language
+    modeling", section "Core mechanism": the probe is rho_i = W_R x_i, a
+    linear map of the layer input like q, k and v. x is [B * L, D] (token
+    rows, sequence b's tokens at rows b L .. b L + L - 1); w stacks
+    [W_Q; W_K; W_V; W_R] as [(2 Hq + 2 Hkv) d, D] rows (output features).
+    Returns q, k, v, r as float64 arrays [B, Hq, L, d], [B, Hkv, L, d],
+    [B, Hkv, L, d], [B, Hq, L, d]: y = x w^T split at the feature
+    boundaries, each part's features grouped into heads of d.
+    """
+    x = _f64(x)
+    w = _f64(w)
+    y = x @ w.T  # [B L, F]
+    bounds = np.cumsum([0, Hq * d, Hkv * d, Hkv * d, Hq * d])
+    outs = []
+    for (lo, hi), H in zip(zip(bounds[:-1], bounds[1:]), (Hq, Hkv, Hkv, Hq)):
+        outs.append(np.ascontiguousarray(y[:, lo:hi].reshape(B, L, H, d).transpose(0, 2, 1, 3)))
+    return tuple(outs)

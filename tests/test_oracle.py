@@ -330,3 +330,55 @@ def test_cor_prefill_and_decode_agree_with_query():
     _, _, dcor = oracle.decode(q[:, :, -1], r[:, :, -1], kc, vc, seqlens, with_cor=True)
     np.testing.assert_allclose(dcor[0], cor[0, :, -1], rtol=0, atol=1e-14)
     assert np.all(dcor[1] == 0.0)
+
+
+# --- the fused probe projection [W_Q; W_K; W_V; W_R] x -----------------------
+
+def test_projection_matches_brute_force_loops():
+    rng = np.random.default_rng(21)
+    B, L, D, Hq, Hkv, d = 2, 3, 5, 2, 1, 2
+    F = (2 * Hq + 2 * Hkv) * d
+    x = rng.normal(size=(B * L, D)); w = rng.normal(size=(F, D))
+    q, k, v, r = oracle.qkvr_projection(x, w, B, L, Hq, Hkv, d)
+    parts = [(q, 0, Hq), (k, Hq * d, Hkv), (v, (Hq + Hkv) * d, Hkv), (r, (Hq + 2 * Hkv) * d, Hq)]
+    for out, base, H in parts:
+        assert out.shape == (B, H, L, d)
+        for b in range(B):
+            for h in range(H):
+                for l in range(L):
+                    for e in range(d):
+                        f = base + h * d + e
+                        ref = sum(x[b * L + l, c] * w[f, c] for c in range(D))
+                        assert abs(out[b, h, l, e] - ref) < 1e-12
+
+
+def test_projection_head_layout_with_selector_weights():
+    """Unit-vector rows make each output element a copy of one input element,
+    so a transposed head or token index shows up exactly."""
+    B, L, Hq, Hkv, d = 2, 4, 2, 1, 3
+    F = (2 * Hq + 2 * Hkv) * d
+    D = F
+    x = np.arange(B * L * D, dtype=np.float64).reshape(B * L, D)
+    w = np.eye(F)
+    q, k, v, r = oracle.qkvr_projection(x, w, B, L, Hq, Hkv, d)
+    assert q[1, 1, 2, 0] == x[1 * L + 2, 1 * d + 0]
+    assert k[0, 0, 3, 2] == x[3, Hq * d + 2]
+    assert v[1, 0, 0, 1] == x[L, (Hq + Hkv) * d + 1]
+    assert r[0, 1, 1, 2] == x[1, (Hq + 2 * Hkv) * d + d + 2]
+
+
+def test_zero_probe_weights_give_softmax_attention():
+    """W_R = 0 (the pages' start for adapting a pretrained model) makes rho
+    zero, and the layer output is then softmax attention."""
+    rng = np.random.default_rng(22)
+    B, L, D, Hq, Hkv, d = 1, 9, 8, 2, 1, 4
+    F = (2 * Hq + 2 * Hkv) * d
+    x = rng.normal(size=(B * L, D)); w = rng.normal(size=(F, D))
+    w[(Hq + 2 * Hkv) * d:] = 0.0
+    q, k, v, r = oracle.qkvr_projection(x, w, B, L, Hq, Hkv, d)
+    assert np.all(r == 0.0)
+    out, _ = oracle.prefill(q, k, v, r)
+    t = [torch.from_numpy(a) for a in (q, k, v)]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        t[0], t[1].repeat_interleave(2, dim=1), t[2].repeat_interleave(2, dim=1), is_causal=True)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=0, atol=1e-12)
