@@ -136,6 +136,25 @@ plx_status plx_prefill_bwd(const void *q, const void *k, const void *v, const vo
                            int Hkv, int L, int d, void *stream);
 
 /*
+ * Fused input projection of a Parallax layer: q, k, v and the probe
+ * rho = W_R x (page "Parallax: parametrized local linear attention for
+ * language modeling", section "Core mechanism") from one product
+ *   y = x [W_Q; W_K; W_V; W_R]^T,
+ * written straight into the per-head layouts the attention calls take.
+ *   x : bf16 [B * L, D]                 token rows; sequence b at rows b L ..
+ *   w : bf16 [(2 Hq + 2 Hkv) d, D]      rows W_Q (Hq d), W_K (Hkv d),
+ *                                       W_V (Hkv d), W_R (Hq d); each
+ *                                       part's rows grouped by head
+ *   q, r : bf16 [B, Hq, L, d];   k, v : bf16 [B, Hkv, L, d]   written
+ * fp32 accumulation, outputs rounded to nearest even. d must be 128, D a
+ * positive multiple of 8; every pointer 16-byte aligned. W_R = 0 (the pages'
+ * start for adapting a pretrained model) gives rho = 0 exactly, and the
+ * layer is then softmax attention.
+ */
+plx_status plx_qkvr_proj(const void *x, const void *w, void *q, void *k, void *v, void *r, int B,
+                         int L, int D, int Hq, int Hkv, int d, void *stream);
+
+/*
  * Causal prefill in fp32 (CUDA cores, fp32 arithmetic throughout). Same
  * arguments and layouts as plx_prefill_fwd with float tensors; d in {64, 128}.
  * This is the exact-arithmetic path used to check parity at 1e-5 relative error.

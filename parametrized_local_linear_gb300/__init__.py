@@ -9,4 +9,5 @@ from .binding import (PlxError, plx_check_device_error, plx_debug_timeout_probe,
                       plx_decode_default_nsplit, plx_decode_fwd, plx_decode_fwd_cor,
                       plx_decode_fwd_noalloc, plx_decode_workspace_bytes,
                       plx_prefill_bwd, plx_prefill_fwd, plx_prefill_fwd_chunk,
-                      plx_prefill_fwd_cor, plx_prefill_fwd_f32, plx_prefill_fwd_train)
+                      plx_prefill_fwd_cor, plx_prefill_fwd_f32, plx_prefill_fwd_train,
+                      plx_qkvr_proj)

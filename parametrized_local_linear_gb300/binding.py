@@ -33,6 +33,7 @@ SIGNATURES = {
     "plx_prefill_fwd_cor": (_i, [_vp] * 7 + [_i] * 6 + [_vp]),
     "plx_prefill_fwd_train": (_i, [_vp] * 8 + [_i] * 5 + [_vp]),
     "plx_prefill_bwd": (_i, [_vp] * 13 + [_i] * 5 + [_vp]),
+    "plx_qkvr_proj": (_i, [_vp] * 6 + [_i] * 6 + [_vp]),
     "plx_decode_fwd": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
     "plx_decode_fwd_ex": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
     "plx_decode_fwd_noalloc": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
@@ -248,6 +249,33 @@ def plx_prefill_bwd(q, k, v, r, out, o1, lse, sbar, dout, dq=None, dk=None, dv=N
                                    dr.data_ptr(), B, Hq, Hkv, L, d, _stream(stream, dev))
     _check(st)
     return dq, dk, dv, dr
+
+
+def plx_qkvr_proj(x, w, B, L, Hq, Hkv, d=128, q=None, k=None, v=None, r=None, stream=None):
+    """Fused [W_Q; W_K; W_V; W_R] x projection (see include/plx.h): x bf16
+    [B * L, D], w bf16 [(2 Hq + 2 Hkv) d, D]. Returns (q, k, v, r) in the
+    attention layouts [B, H, L, d]."""
+    _need(x, "x", torch.bfloat16, 2)
+    dev = x.device
+    _need(w, "w", torch.bfloat16, 2, dev)
+    T, D = x.shape
+    if T != B * L or tuple(w.shape) != ((2 * Hq + 2 * Hkv) * d, D):
+        raise ValueError("x must be [B * L, D] and w [(2 Hq + 2 Hkv) d, D]")
+    shapes = {"q": (B, Hq, L, d), "k": (B, Hkv, L, d), "v": (B, Hkv, L, d), "r": (B, Hq, L, d)}
+    outs = {}
+    for name, t in (("q", q), ("k", k), ("v", v), ("r", r)):
+        if t is None:
+            t = torch.empty(shapes[name], dtype=torch.bfloat16, device=dev)
+        _need(t, name, torch.bfloat16, 4, dev)
+        if tuple(t.shape) != shapes[name]:
+            raise ValueError(f"{name} must be {shapes[name]}")
+        outs[name] = t
+    with torch.cuda.device(dev):
+        st = lib().plx_qkvr_proj(x.data_ptr(), w.data_ptr(), outs["q"].data_ptr(),
+                                 outs["k"].data_ptr(), outs["v"].data_ptr(), outs["r"].data_ptr(),
+                                 B, L, D, Hq, Hkv, d, _stream(stream, dev))
+    _check(st)
+    return outs["q"], outs["k"], outs["v"], outs["r"]
 
 
 def plx_prefill_fwd_f32(q, k, v, r, out=None, lse=None, stream=None):

@@ -229,6 +229,27 @@ plx_status plx_prefill_fwd_f32(const float *q, const float *k, const float *v, c
                        fn);
 }
 
+plx_status plx_qkvr_proj(const void *x, const void *w, void *q, void *k, void *v, void *r, int B,
+                         int L, int D, int Hq, int Hkv, int d, void *stream) {
+  const char *fn = "plx_qkvr_proj";
+  if (!x || !w || !q || !k || !v || !r) return fail(PLX_ERR_INVALID_ARG, "%s: null pointer", fn);
+  plx_status s = check_common(fn, B, Hq, Hkv, L, d);
+  if (s) return s;
+  if (D < 1 || D % 8 != 0)
+    return fail(PLX_ERR_INVALID_ARG, "%s: model dim %d must be a positive multiple of 8", fn, D);
+  if (d != 128) return fail(PLX_ERR_UNSUPPORTED, "%s: head dim %d (only 128)", fn, d);
+  const void *ptrs[] = {x, w, q, k, v, r};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return fail(PLX_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
+  if (static_cast<long long>(B) * L > 0x7fffffffLL - 128 ||
+      static_cast<long long>(2 * Hq + 2 * Hkv) * d > 0x7fffffffLL)
+    return fail(PLX_ERR_UNSUPPORTED, "%s: problem too large for one launch", fn);
+  return finish_launch(plx::launch_qkvr_proj(x, w, q, k, v, r, B, L, D, Hq, Hkv,
+                                             plx::device_error_word(),
+                                             static_cast<cudaStream_t>(stream)),
+                       fn);
+}
+
 size_t plx_decode_workspace_bytes(int B, int Hq, int d, int nsplit) {
   if (B < 1 || Hq < 1 || d < 1 || nsplit < 1) return 0;
   return static_cast<size_t>(B) * Hq * nsplit * (2 * static_cast<size_t>(d) + 2) * sizeof(float);

@@ -57,6 +57,11 @@ constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;
 // Device address of that array on the current device (resolved once per device).
 cudaError_t noalloc_scratch(float **ptr);
 
+// Fused [W_Q; W_K; W_V; W_R] x projection into per-head q, k, v, r (d = 128).
+cudaError_t launch_qkvr_proj(const void *x, const void *w, void *q, void *k, void *v, void *r,
+                             int B, int L, int D, int Hq, int Hkv, unsigned *err,
+                             cudaStream_t stream);
+
 cudaError_t launch_timeout_probe(long long limit_cycles, unsigned *err, cudaStream_t stream);
 
 }  // namespace plx
