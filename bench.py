@@ -409,6 +409,17 @@ def main():
                launch_s(lambda: plx_prefill_bwd(q, k, v, r, o_t, o1_t, lse_t, sb_t, do_t,
                                                 gq, gk, gv, gr), 10))
         del o_t, lse_t, o1_t, sb_t, do_t, gq, gk, gv, gr
+        # The fused input projection x [W_Q; W_K; W_V; W_R]^T of the 0.6B- and
+        # 1.7B-shaped layers (model dims 1024 and 2048), all B L tokens.
+        from parametrized_local_linear_gb300 import plx_qkvr_proj
+        for dm, tag in ((1024, "0p6b"), (2048, "1p7b")):
+            F = (2 * wp.Hq + 2 * wp.Hkv) * wp.d
+            xt = torch.randn(wp.B * wp.L, dm, device=dev).to(torch.bfloat16)
+            wt = (torch.randn(F, dm, device=dev) / dm ** 0.5).to(torch.bfloat16)
+            po = [torch.empty_like(t) for t in (q, k, v, r)]
+            tflops(f"qkvr_projection_{tag}_T{wp.B * wp.L}_D{dm}_F{F}", 2 * wp.B * wp.L * dm * F,
+                   launch_s(lambda: plx_qkvr_proj(xt, wt, wp.B, wp.L, wp.Hq, wp.Hkv, wp.d, *po), 10))
+            del xt, wt, po
         w5 = inputs.DECODE_RAGGED
         d5 = inputs.decode_inputs_for(w5, device=dev)
         sl5 = d5[4].to(dev)
