@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # captures summarised in profiles/ (prefill: the bench's own workload;
 # decode: a quarter-size batch scaled by 4, the traffic being proportional to
 # the cache streamed). Set to None whenever a kernel changes after its capture.
-NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": None, "decode_split_kernel": 4 * 543.9e6}
+NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": 376.4e6, "decode_split_kernel": 4 * 543.9e6}
 
 
 def load_peaks():
@@ -215,6 +215,21 @@ def run_ncu_case(case):
         q, k, v, r = inputs.prefill_inputs_for(w, device=dev)
         out = torch.empty_like(q)
         fn = lambda: plx_prefill_fwd(q, k, v, r, out)  # noqa: E731
+    elif case == "backward":
+        from parametrized_local_linear_gb300 import plx_prefill_bwd, plx_prefill_fwd_train
+        w = inputs.PREFILL_0P6B  # about 0.6 GB of inputs, saved tensors and gradients
+        q, k, v, r = inputs.prefill_inputs_for(w, device=dev)
+        o, lse, o1, sb = plx_prefill_fwd_train(q, k, v, r)
+        do = torch.randn(q.shape, device=dev).to(q.dtype)
+        g = [torch.empty_like(x) for x in (q, k, v, r)]
+        fn = lambda: plx_prefill_bwd(q, k, v, r, o, o1, lse, sb, do, *g)  # noqa: E731
+    elif case == "projection":
+        from parametrized_local_linear_gb300 import plx_qkvr_proj
+        w = inputs.PREFILL_0P6B  # x 32 MB, W 12 MB, q/k/v/r 201 MB
+        F = (2 * w.Hq + 2 * w.Hkv) * w.d
+        x = torch.randn(w.B * w.L, 1024, device=dev).to(torch.bfloat16)
+        wt = (torch.randn(F, 1024, device=dev) / 32.0).to(torch.bfloat16)
+        fn = lambda: plx_qkvr_proj(x, wt, w.B, w.L, w.Hq, w.Hkv, w.d)  # noqa: E731
     else:
         if case == "decode":
             lens = [8192] * 16  # 16 x 8192 tokens x 8 heads: 537 MB of cache
@@ -241,7 +256,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the 1.7B / ragged timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_ragged"], default=None,
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_ragged", "backward",
+                                           "projection"], default=None,
                     help="run 3 warm-up + 3 launches of one kernel on a profiling-sized case "
                          "(inputs > L2, < 1 GB) and exit; prints nothing")
     args = ap.parse_args()
