@@ -381,33 +381,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint64_t v) {
   return r;
 }
 
-// 2^x for a pair of x <= 8 on the FMA pipe instead of the MUFU unit, so the
-// two can share the exponentials. Round-to-nearest range reduction x = n + f,
-// |f| <= 1/2, with the 1.5 * 2^23 shift (n then sits in the low mantissa
-// bits of x + 1.5 * 2^23), then a degree-4 polynomial for 2^f and n added to
-// the exponent field. The coefficients are our own weighted least-squares
-// (Lawson) fit of 2^f on [-1/2, 1/2] for minimum relative error; evaluated in
-// fp32 the result is within 3e-6 relative of 2^x for x in [-125, 8]. Inputs
-// below -125 (including -inf) are clamped there: 2^-125 is zero for every
-// use here.
-__device__ __forceinline__ uint64_t exp2_poly2(uint64_t x) {
-  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  const uint64_t xc = f2(fmaxf(f2lo(x), -125.f), fmaxf(f2hi(x), -125.f));
-  const uint64_t t = fadd2(xc, f2(kShift, kShift));
-  const uint64_t r = fadd2(t, f2(-kShift, -kShift));
-  const uint64_t f = ffma2(r, f2(-1.f, -1.f), xc);
-  uint64_t p = ffma2(f2(0.009570102207362652f, 0.009570102207362652f), f,
-                     f2(0.05591786280274391f, 0.05591786280274391f));
-  p = ffma2(p, f, f2(0.240247443318367f, 0.240247443318367f));
-  p = ffma2(p, f, f2(0.6931217908859253f, 0.6931217908859253f));
-  p = ffma2(p, f, f2(0.9999992847442627f, 0.9999992847442627f));
-  // n = bits(t) - bits(1.5 * 2^23); add n << 23 to the exponent field.
-  const uint32_t off = 0x4B400000u << 23;
-  const uint32_t lo = __float_as_uint(f2lo(p)) + (__float_as_uint(f2lo(t)) << 23) - off;
-  const uint32_t hi = __float_as_uint(f2hi(p)) + (__float_as_uint(f2hi(t)) << 23) - off;
-  return f2(__uint_as_float(lo), __uint_as_float(hi));
-}
-
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

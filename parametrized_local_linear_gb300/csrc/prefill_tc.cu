@@ -335,9 +335,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           m_used = mt;
         }
         const float msub = m_used == -INFINITY ? 0.f : m_used;
-        // Pairs of columns in packed fp32; one pair in four takes its
-        // exponentials from the FMA-pipe polynomial, the rest from MUFU, which
-        // balances the two units (MUFU alone was the softmax's bottleneck).
+        // Pairs of columns in packed fp32; exponentials from MUFU (ex2).
         const uint64_t c2 = f2(c, c), nm2 = f2(-msub, -msub);
         uint64_t lp[2] = {f2(0.f, 0.f), f2(0.f, 0.f)}, sp[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
@@ -354,8 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int e = 0; e < 16; e += 2) {
             const int col = 16 * qq + e;
             const uint64_t xx = ffma2(f2(s[col], s[col + 1]), c2, nm2);
-            const uint64_t p = ((col >> 1) & 3) == 3 ? exp2_poly2(xx)
-                                                     : f2(fast_exp2(f2lo(xx)), fast_exp2(f2hi(xx)));
+            const uint64_t p = f2(fast_exp2(f2lo(xx)), fast_exp2(f2hi(xx)));
             const uint64_t pt = fmul2(p, f2(t[e], t[e + 1]));
             lp[(e >> 1) & 1] = fadd2(lp[(e >> 1) & 1], p);
             sp[(e >> 1) & 1] = fadd2(sp[(e >> 1) & 1], pt);
