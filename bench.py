@@ -171,6 +171,52 @@ def oracle_prefill_sample(w, q, k, v, r, budget_s, seed, threads=None):
     return done_flops, secs, rows_done, threads
 
 
+def oracle_extra_samples(w, q, k, v, r, budget_s, seed=12):
+    """The gradient and projection oracles timed on bounded samples of the
+    0.6B-shaped workload: {row name: cpu_baseline dict}."""
+    import random
+
+    import numpy as np
+
+    import oracle
+    from oracle import grad as ograd
+    rng = random.Random(seed)
+    out = {}
+    # Gradient oracle: whole gradients of random causal rows (autograd through
+    # the explicit Sigma of the row), 16 d flops per (query, key) pair.
+    dout = torch.randn(q.shape[2:], device=q.device).to(q.dtype)
+    flops, secs, n = 0, 0.0, 0
+    while secs < budget_s:
+        b, h, i = rng.randrange(w.B), rng.randrange(w.Hq), rng.randrange(w.L)
+        g = h // (w.Hq // w.Hkv)
+        args = [q[b, h, i].cpu(), r[b, h, i].cpu(), k[b, g, :i + 1].cpu(), v[b, g, :i + 1].cpu(),
+                dout[i].cpu()]
+        ts = time.perf_counter()
+        ograd.row_grads(*args)
+        secs += time.perf_counter() - ts
+        flops += 16 * w.d * (i + 1)
+        n += 1
+    out[w.name + "_backward"] = {
+        "value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
+        "kind": "oracle", "sample": f"whole gradients of {n} random causal rows (torch fp64 "
+                                    f"autograd through explicit Sigma), {secs:.1f} s"}
+    # Projection oracle: fp64 product for random token rows of the layer.
+    D, F = 1024, (2 * w.Hq + 2 * w.Hkv) * w.d
+    xs = np.random.default_rng(seed).standard_normal((256, D))
+    ws = np.random.default_rng(seed + 1).standard_normal((F, D))
+    flops, secs, n = 0, 0.0, 0
+    while secs < budget_s / 4:
+        ts = time.perf_counter()
+        oracle.qkvr_projection(xs, ws, 1, xs.shape[0], w.Hq, w.Hkv, w.d)
+        secs += time.perf_counter() - ts
+        flops += 2 * xs.shape[0] * D * F
+        n += xs.shape[0]
+    out[f"qkvr_projection_0p6b_T{w.B * w.L}_D{D}_F{F}"] = {
+        "value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
+        "kind": "oracle", "sample": f"{n} token rows (numpy fp64 product), {secs:.1f} s"}
+    return out
+
+
 def run_reference(args, world, rank):
     """The oracle as the reference arm: each step is a bounded row sample."""
     if rank != 0:
@@ -457,6 +503,10 @@ def main():
         cpu = {"value": f / secs / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} random causal rows of {wp.name} (explicit Sigma_KV, fp64), "
                          f"{secs:.1f} s"}
+        if extra:
+            for name, base in oracle_extra_samples(wp, q, k, v, r, args.cpu_seconds / 4).items():
+                if name in extra:
+                    extra[name]["cpu_baseline"] = base
 
     clocks = clk.summary()
     line = {
