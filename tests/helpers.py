@@ -87,13 +87,14 @@ def assert_cor_close(got, ref, what=""):
 GRAD_REL = 1e-2
 
 
-def assert_grad_close(got, ref, what=""):
+def assert_grad_close(got, ref, what="", scale=None):
+    """max|err| <= GRAD_REL * scale, scale = max|ref| unless given."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite gradient"
     err = np.max(np.abs(got - ref))
-    scale = np.max(np.abs(ref))
+    scale = np.max(np.abs(ref)) if scale is None else scale
     print(f"{what}: max|err| / max|ref| = {err / scale:.3e}")
     assert err <= GRAD_REL * scale, f"{what}: max|err| {err:.3e} > {GRAD_REL} * {scale:.3e}"
     return err / scale

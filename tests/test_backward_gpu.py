@@ -47,6 +47,9 @@ def test_train_forward_saves_osa_and_sbar():
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,L", [
+    (1, 2, 1, 1),      # one token: Sigma = 0, the softmax has one weight
+    (2, 2, 1, 2),      # two tokens
+    (1, 2, 1, 65),     # one key block, a 1-row second query tile
     (1, 2, 1, 200),    # ragged last query and key tiles
     (2, 4, 2, 130),    # GQA pairs, just over one 128-row block
     (1, 2, 2, 64),     # one key tile, no GQA
@@ -56,8 +59,14 @@ def test_backward_matches_oracle(B, Hq, Hkv, L):
     q, k, v, r, do = _case(B, Hq, Hkv, L, 50 + L)
     got = _gpu_grads(q, k, v, r, do)
     want = ograd.prefill_grad(q, k, v, r, do)
+    # With one or two keys per row the exact score and probe gradients vanish
+    # or nearly so (one key: dq = dk = drho = 0, dv = dout), while the kernel
+    # carries the forward's bf16 rounding of P o T (O2 uses the rounded
+    # product, sigma the fp32 one). There the error is measured against the
+    # largest gradient of the step instead of each tensor's own largest.
+    scale = max(float(w_.abs().max()) for w_ in want) if L <= 2 else None
     for name, g_, w_ in zip(("dq", "dk", "dv", "dr"), got, want):
-        assert_grad_close(g_.numpy(), w_.numpy(), f"{name} B{B} Hq{Hq} Hkv{Hkv} L{L}")
+        assert_grad_close(g_.numpy(), w_.numpy(), f"{name} B{B} Hq{Hq} Hkv{Hkv} L{L}", scale=scale)
 
 
 def test_backward_is_deterministic():
@@ -94,3 +103,27 @@ def test_backward_full_size_sampled():
     want_v = do.double().sum(2).reshape(w.B, w.Hkv, G, w.d).sum(2)
     scale_v = dv.abs().sum(2)
     assert torch.all((dv.sum(2) - want_v).abs() <= 2e-3 * scale_v + 1e-3)
+
+
+def test_backward_1p7b_shape_sampled():
+    """The 1.7B-shaped prefill (B = 1, L = 16384): dq, dr on sampled rows and
+    dk, dv on the last keys against the oracle, shift invariants over all keys."""
+    w = inputs.PREFILL_1P7B
+    q, k, v, r = inputs.prefill_inputs_for(w)
+    g = torch.Generator().manual_seed(w.seed + 7)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    dq, dk, dv, dr = _gpu_grads(q, k, v, r, do)
+    rows = sample_rows(w.B, w.Hq, w.L, n_random=4, seed=w.seed)
+    rq, rr = ograd.prefill_grad_rows(q, k, v, r, do, rows)
+    idx = tuple(torch.as_tensor(x) for x in np.array(rows).T)
+    assert_grad_close(dq[idx].numpy(), rq.numpy(), "dq rows (1.7B)")
+    assert_grad_close(dr[idx].numpy(), rr.numpy(), "dr rows (1.7B)")
+    keys = [(0, 0, w.L - 1), (0, 5, w.L - 3)]
+    rk, rv = ograd.prefill_grad_keys(q, k, v, r, do, keys)
+    kidx = tuple(torch.as_tensor(x) for x in np.array(keys).T)
+    assert_grad_close(dk[kidx].numpy(), rk.numpy(), "dk last keys (1.7B)")
+    assert_grad_close(dv[kidx].numpy(), rv.numpy(), "dv last keys (1.7B)")
+    G = w.Hq // w.Hkv
+    assert torch.all(dk.sum(2).abs() <= 2e-3 * dk.abs().sum(2) + 1e-3)
+    want_v = do.double().sum(2).reshape(w.B, w.Hkv, G, w.d).sum(2)
+    assert torch.all((dv.sum(2) - want_v).abs() <= 2e-3 * dv.abs().sum(2) + 1e-3)

@@ -43,7 +43,9 @@ def _check_rounding(got, ref, what):
 
 
 @pytest.mark.parametrize("B,L,D,Hq,Hkv", [
+    (1, 1, 64, 1, 1),        # a single token
     (1, 128, 64, 1, 1),      # one tile of each kind
+    (3, 129, 2048, 1, 1),    # an odd number of token tiles (the cluster's last partner is empty)
     (2, 200, 1024, 2, 1),    # a 128-row tile straddles the two sequences
     (1, 77, 200, 3, 1),      # token tail and a K tail (200 = 3 x 64 + 8)
     (3, 50, 512, 4, 2),      # several sequences inside one tile
@@ -58,10 +60,11 @@ def test_projection_matches_oracle(B, L, D, Hq, Hkv):
         _check_rounding(got.double().cpu().numpy(), ref, name)
 
 
-def test_projection_full_size_sampled_tokens():
-    """The 0.6B-shaped layer (model dim 1024, 16 query and 8 kv heads,
-    B = 4, L = 4096) on sampled token rows."""
-    B, L, D, Hq, Hkv = 4, 4096, 1024, 16, 8
+@pytest.mark.parametrize("D", [1024, 2048])
+def test_projection_full_size_sampled_tokens(D):
+    """The 0.6B- and 1.7B-shaped layers (model dims 1024 and 2048, 16 query
+    and 8 kv heads, B = 4, L = 4096 tokens) on sampled token rows."""
+    B, L, Hq, Hkv = 4, 4096, 16, 8
     dev = device()
     x, w = _inputs(B, L, D, Hq, Hkv, 7)
     q, k, v, r = plx_qkvr_proj(x.to(dev), w.to(dev), B, L, Hq, Hkv)
