@@ -366,25 +366,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         l += f2lo(lsum) + f2hi(lsum);
         sg += f2lo(ssum) + f2hi(ssum);
         tmem_wait_st();
-        if (j > 0) {
-          // The previous tile's value UMMAs must be done before O is touched
-          // and before P of this tile is handed over.
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // Rescaling O: the previous tile's value UMMAs must be done first.
+          // Without a rescale P is handed over at once; the value UMMAs of
+          // one accumulator run in issue order, so tile j's follow tile j-1's.
           ok = mbar_wait(smem_u32(&pv_done[(gg - 1) & 1]), ((gg - 1) >> 1) & 1, ab);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, need)) {
-  #pragma unroll 1
-            for (int part = 0; part < 8; ++part) {
-              const uint32_t col = (part < 4 ? COL_O1 : COL_O2) + (part & 3) * 32;
-              float o[32];
-              tmem_ld32(tl + col, o);
-              tmem_wait_ld();
-  #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= alpha;
-              tmem_st32(tl + col, o);
-            }
-            tmem_wait_st();
+#pragma unroll 1
+          for (int part = 0; part < 8; ++part) {
+            const uint32_t col = (part < 4 ? COL_O1 : COL_O2) + (part & 3) * 32;
+            float o[32];
+            tmem_ld32(tl + col, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tl + col, o);
           }
+          tmem_wait_st();
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&p_full[x]));
