@@ -45,7 +45,10 @@
 //   [256,384) O1              [384,512) O2
 // The softmax writes P and P o T as packed bf16 (S_x[0,32) = P, T_x[0,32) =
 // P o T) and the value GEMMs read them straight from TMEM (A-from-TMEM
-// form), V from shared memory (MN-major). Rescaling is lazy: the max used in
+// form), V from shared memory (MN-major). P is handed over in two halves of
+// 32 keys, so the first two K steps of the value UMMAs start while the
+// softmax still works on the second half; an O rescale (rare with the lazy
+// max) happens before either half is handed over. Rescaling is lazy: the max used in
 // the exponent only moves when a row's tile max exceeds it by more than
 // 2^8, which keeps every quantity exact (they all share the stale max) and
 // rarely touches O in TMEM.
@@ -70,7 +73,7 @@ constexpr int OFF_K = 4 * HALF_Q;             // 65536
 constexpr int OFF_V = OFF_K + NST * TILE_KV;  // 131072
 constexpr int OFF_STAT = OFF_V + NST * TILE_KV;  // 196608: [2][3][BM] row statistics
 constexpr int OFF_BAR = OFF_STAT + 2 * 3 * BM * 4;
-constexpr int NBAR = 2 + 4 * NST + 2 + 2 + 2 + 1 + 2 + 4;
+constexpr int NBAR = 2 + 4 * NST + 2 + 4 + 2 + 1 + 2 + 4;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
 constexpr int SM_WARP0 = 3;                   // first softmax warp
 constexpr int EP_WARP0 = 9;                   // first epilogue warp
@@ -128,8 +131,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *v_full = k_empty + NST;
   uint64_t *v_empty = v_full + NST;    // count 2 (O1 and O2)
   uint64_t *st_full = v_empty + NST;   // [2] count 2
-  uint64_t *p_full = st_full + 2;      // [2] count 128
-  uint64_t *pv_done = p_full + 2;      // [2] count 2: value UMMAs of the tiles in buffer x
+  uint64_t *p_full = st_full + 2;      // [2][2] count 128: P of keys [32 h, 32 h + 32) of buffer x
+  uint64_t *pv_done = p_full + 4;      // [2] count 2: value UMMAs of the tiles in buffer x
   uint64_t *o_free = pv_done + 2;      // count 128: the epilogue has read O1 and O2
   uint64_t *stat_full = o_free + 1;    // [2] count 128: row statistics of an item written
   uint64_t *drain = stat_full + 2;     // [4]: one per issuing thread
@@ -149,7 +152,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&st_full[x]), 2);
-      mbar_init(smem_u32(&p_full[x]), 128);
+      mbar_init(smem_u32(&p_full[2 * x]), 128);
+      mbar_init(smem_u32(&p_full[2 * x + 1]), 128);
       mbar_init(smem_u32(&pv_done[x]), 2);
       mbar_init(smem_u32(&stat_full[x]), 128);
     }
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int k = 0; ok && item_of(a, k, it); ++k) {
         for (int j = 0; j < it.ntiles; ++j) {
           const int gg = g + j, x = gg & 1, st = gg % NST;
-          if (!mbar_wait(smem_u32(&p_full[x]), (gg >> 1) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&p_full[2 * x]), (gg >> 1) & 1, ab)) { ok = false; break; }
           // The first value UMMA of an item overwrites O: the previous item's
           // epilogue must have read it.
           if (j == 0 && k > 0 && !mbar_wait(smem_u32(o_free), (k - 1) & 1, ab)) { ok = false; break; }
@@ -242,8 +246,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t vdesc = vdesc0 + st * (TILE_KV >> 4);
           const uint32_t ap = tbase + (x ? COL_S1 : COL_S0) + col_off;
 #pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks)
+          for (int ks = 0; ks < BN / 16; ++ks) {
+            if (ks == 2 && !mbar_wait(smem_u32(&p_full[2 * x + 1]), (gg >> 1) & 1, ab)) { ok = false; break; }
             umma_ts(dout, ap + ks * 8, vdesc + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0));
+          }
+          if (!ok) break;
           umma_commit(smem_u32(&pv_done[x]));
           umma_commit(smem_u32(&v_empty[st]));
         }
@@ -334,6 +341,26 @@ __global__ void __launch_bounds__(THREADS, 1)
           sg *= alpha;
           m_used = mt;
         }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // Rescaling O: the previous tile's value UMMAs must be done first.
+          // Without a rescale P is handed over as soon as it is written; the
+          // value UMMAs of one accumulator run in issue order, so tile j's
+          // follow tile j-1's.
+          ok = mbar_wait(smem_u32(&pv_done[(gg - 1) & 1]), ((gg - 1) >> 1) & 1, ab);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int part = 0; part < 8; ++part) {
+            const uint32_t col = (part < 4 ? COL_O1 : COL_O2) + (part & 3) * 32;
+            float o[32];
+            tmem_ld32(tl + col, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tl + col, o);
+          }
+          tmem_wait_st();
+        }
         const float msub = m_used == -INFINITY ? 0.f : m_used;
         // Pairs of columns in packed fp32; exponentials from MUFU (ex2).
         const uint64_t c2 = f2(c, c), nm2 = f2(-msub, -msub);
@@ -361,32 +388,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tmem_st8(cs + 8 * qq, pk);
           tmem_st8(cs + COL_T + 8 * qq, ptk);
+          if (qq == 1) {
+            // P of keys [0, 32) is in place: its value UMMAs may start.
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&p_full[2 * x]));
+          }
         }
         const uint64_t lsum = fadd2(lp[0], lp[1]), ssum = fadd2(sp[0], sp[1]);
         l += f2lo(lsum) + f2hi(lsum);
         sg += f2lo(ssum) + f2hi(ssum);
         tmem_wait_st();
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // Rescaling O: the previous tile's value UMMAs must be done first.
-          // Without a rescale P is handed over at once; the value UMMAs of
-          // one accumulator run in issue order, so tile j's follow tile j-1's.
-          ok = mbar_wait(smem_u32(&pv_done[(gg - 1) & 1]), ((gg - 1) >> 1) & 1, ab);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll 1
-          for (int part = 0; part < 8; ++part) {
-            const uint32_t col = (part < 4 ? COL_O1 : COL_O2) + (part & 3) * 32;
-            float o[32];
-            tmem_ld32(tl + col, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(tl + col, o);
-          }
-          tmem_wait_st();
-        }
         tc_fence_before();
-        mbar_arrive(smem_u32(&p_full[x]));
+        mbar_arrive(smem_u32(&p_full[2 * x + 1]));
       }
       if (!ok) break;
       // Hand the row statistics to the epilogue and move on to the next item.
