@@ -37,9 +37,13 @@
 // as the tensor core retires these shapes (measured: 50-100 cycles per issue
 // under load against 48-64 cycles of work per instruction). The value
 // UMMAs, which sit on the critical path (softmax -> P V -> next softmax), have
-// issuers of their own that respond at once; S and T of tile j + 2 overwrite
-// P(j) and P o T(j) and therefore wait for the value UMMAs of tile j
-// (pv_done), which leaves them two tiles of slack.
+// issuers of their own that respond at once. S and T of tile j + 2 overwrite
+// P(j) and P o T(j), so they must execute after the value UMMAs of tile j:
+// each value issuer signals pv_issued once its UMMAs are issued (after a
+// tcgen05 before-thread-sync fence), and the score issuer waits for that
+// signal (then an after-thread-sync fence) and issues behind them. The
+// tensor pipe executes UMMAs in that order, so the score UMMAs queue right
+// behind the value UMMAs instead of waiting for them to complete.
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,64) S_0  [64,128) T_0  [128,192) S_1  [192,256) T_1  (double buffered)
 //   [256,384) O1              [384,512) O2
@@ -73,7 +77,7 @@ constexpr int OFF_K = 4 * HALF_Q;             // 65536
 constexpr int OFF_V = OFF_K + NST * TILE_KV;  // 131072
 constexpr int OFF_STAT = OFF_V + NST * TILE_KV;  // 196608: [2][3][BM] row statistics
 constexpr int OFF_BAR = OFF_STAT + 2 * 3 * BM * 4;
-constexpr int NBAR = 2 + 4 * NST + 2 + 4 + 2 + 1 + 2 + 4;
+constexpr int NBAR = 2 + 4 * NST + 2 + 4 + 2 + 4 + 1 + 2 + 4;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
 constexpr int SM_WARP0 = 3;                   // first softmax warp
 constexpr int EP_WARP0 = 9;                   // first epilogue warp
@@ -133,7 +137,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *st_full = v_empty + NST;   // [2] count 2
   uint64_t *p_full = st_full + 2;      // [2][2] count 128: P of keys [32 h, 32 h + 32) of buffer x
   uint64_t *pv_done = p_full + 4;      // [2] count 2: value UMMAs of the tiles in buffer x
-  uint64_t *o_free = pv_done + 2;      // count 128: the epilogue has read O1 and O2
+  uint64_t *pv_issued = pv_done + 2;   // [2][2]: O1 (h = 0) / O2 (h = 1) value UMMAs of buffer x issued
+  uint64_t *o_free = pv_issued + 4;      // count 128: the epilogue has read O1 and O2
   uint64_t *stat_full = o_free + 1;    // [2] count 128: row statistics of an item written
   uint64_t *drain = stat_full + 2;     // [4]: one per issuing thread
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
@@ -155,6 +160,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&p_full[2 * x]), 128);
       mbar_init(smem_u32(&p_full[2 * x + 1]), 128);
       mbar_init(smem_u32(&pv_done[x]), 2);
+      mbar_init(smem_u32(&pv_issued[2 * x]), 1);
+      mbar_init(smem_u32(&pv_issued[2 * x + 1]), 1);
       mbar_init(smem_u32(&stat_full[x]), 128);
     }
     mbar_init(smem_u32(o_free), 128);
@@ -253,6 +260,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!ok) break;
           umma_commit(smem_u32(&pv_done[x]));
           umma_commit(smem_u32(&v_empty[st]));
+          // The score UMMAs of tile gg + 2 may now be issued behind these.
+          tc_fence_before();
+          mbar_arrive(smem_u32(&pv_issued[2 * x + (is_o1 ? 0 : 1)]));
         }
         g += it.ntiles;
       }
@@ -278,9 +288,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(smem_u32(q_full), k & 1, ab)) break;
         for (int j = 0; j < it.ntiles; ++j) {
           const int gg = g + j, x = gg & 1, st = gg % NST;
-          // Buffer x still holds P / P o T of CTA tile gg - 2 until its value
-          // UMMAs finish.
-          if (gg >= 2 && !mbar_wait(smem_u32(&pv_done[x]), ((gg - 2) >> 1) & 1, ab)) { ok = false; break; }
+          // Buffer x holds P (P o T) of CTA tile gg - 2: its value UMMAs must
+          // have been issued; issued earlier, they execute first.
+          if (gg >= 2 && !mbar_wait(smem_u32(&pv_issued[2 * x + (is_s ? 0 : 1)]), ((gg - 2) >> 1) & 1, ab)) { ok = false; break; }
           if (!mbar_wait(smem_u32(&k_full[st]), (gg / NST) & 1, ab)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kdesc = kdesc0 + st * (TILE_KV >> 4);
