@@ -380,24 +380,54 @@ def main():
     hbm_peak = _peak(peaks, "hbm_gbs")
 
     # ---------------------------------------------------------------- e2e
-    # Through the same C-ABI call, from pinned host buffers: H2D of q, k, v, r,
-    # the prefill, D2H of out (and the decode step likewise) inside the timing.
+    # Through the same C-ABI calls, from pinned host buffers, with the copies
+    # inside the timing: each sequence's q, k, v, r go to the device on a copy
+    # stream while the previous sequence's prefill runs (one plx_prefill_fwd
+    # call per sequence), the decode's new q, r follow, and each output comes
+    # back while later work runs. A step ends when its last copy has landed.
     hq = [t.cpu().pin_memory() for t in (q, k, v, r)]
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hd = [t.cpu().pin_memory() for t in (dq, dr)]
     hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in hq + hd)
     d2h = hout.numel() * hout.element_size() + hdout.numel() * hdout.element_size()
+    nseq = q.shape[0]
+    copy_stream = torch.cuda.Stream(dev)
+    dseq = [[torch.empty_like(t[b:b + 1]) for t in (q, k, v, r)] for b in range(nseq)]
+    dseq_out = [torch.empty_like(out[b:b + 1]) for b in range(nseq)]
+    ddec = [torch.empty_like(t) for t in (dq, dr)]
+    ddec_out = torch.empty_like(dout)
 
     def e2e_step():
-        dq_ = [t.to(dev, non_blocking=True) for t in hq]
-        o_ = torch.empty_like(dq_[0])
-        plx_prefill_fwd(*dq_, o_)
-        hout.copy_(o_, non_blocking=True)
-        dd_ = [t.to(dev, non_blocking=True) for t in hd]
-        od_ = torch.empty_like(dd_[0])
-        plx_decode_fwd(dd_[0], dd_[1], kc, vc, sl, od_)
-        hdout.copy_(od_, non_blocking=True)
+        ev_in = []
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_stream(stream)  # the previous step is done with the buffers
+            for b in range(nseq):
+                for dst, src in zip(dseq[b], hq):
+                    dst.copy_(src[b:b + 1], non_blocking=True)
+                ev_in.append(torch.cuda.Event())
+                ev_in[-1].record(copy_stream)
+            for dst, src in zip(ddec, hd):
+                dst.copy_(src, non_blocking=True)
+            ev_dec = torch.cuda.Event()
+            ev_dec.record(copy_stream)
+        ev_out = []
+        for b in range(nseq):
+            stream.wait_event(ev_in[b])
+            plx_prefill_fwd(*dseq[b], dseq_out[b])
+            ev_out.append(torch.cuda.Event())
+            ev_out[-1].record(stream)
+        stream.wait_event(ev_dec)
+        plx_decode_fwd(ddec[0], ddec[1], kc, vc, sl, ddec_out)
+        ev_d = torch.cuda.Event()
+        ev_d.record(stream)
+        with torch.cuda.stream(copy_stream):
+            for b in range(nseq):
+                copy_stream.wait_event(ev_out[b])
+                hout[b:b + 1].copy_(dseq_out[b], non_blocking=True)
+            copy_stream.wait_event(ev_d)
+            hdout.copy_(ddec_out, non_blocking=True)
+        stream.wait_stream(copy_stream)
 
     for _ in range(2):
         e2e_step()
@@ -410,6 +440,9 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / ke
+    # Per-sequence calls give bit-for-bit the batched call's output.
+    if not torch.equal(hout, out.cpu()):
+        raise RuntimeError("e2e prefill output differs from the batched call")
     # The e2e step also contains the decode; count its time, credit only prefill flops.
     e2e_value = world * wp.flops / (e2e_ms * 1e-3) / 1e12
 
@@ -543,7 +576,9 @@ def main():
         "extra": extra,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "method": "one prefill call per sequence; host copies on a second stream, "
+                          "overlapped with the kernels, inside the timing"},
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev),
