@@ -85,3 +85,39 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(binding, "LIB_PATH", "/nonexistent/libplx.so")
     with pytest.raises(RuntimeError, match="not built"):
         binding.lib()
+
+
+def test_chunk_cor_and_train_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(4096)
+    chunk = lib.plx_prefill_fwd_chunk
+    assert chunk(p, p, p, p, p, None, 1, 2, 1, 64, 32, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert b"Lk" in lib.plx_last_error_message()
+    assert chunk(p, p, p, p, p, None, 1, 2, 1, 16, 64, 64, None) == binding.PLX_ERR_UNSUPPORTED
+    cor = lib.plx_prefill_fwd_cor
+    assert cor(p, p, p, p, p, None, None, 1, 2, 1, 16, 16, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert b"cor" in lib.plx_last_error_message()
+    train = lib.plx_prefill_fwd_train
+    assert train(p, p, p, p, p, p, None, p, 1, 2, 1, 16, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert b"o1" in lib.plx_last_error_message()
+    assert train(p, p, p, p, p, p, ctypes.c_void_p(4098), p, 1, 2, 1, 16, 128,
+                 None) == binding.PLX_ERR_INVALID_ARG
+    assert b"aligned" in lib.plx_last_error_message()
+    dcor = lib.plx_decode_fwd_cor
+    assert dcor(p, p, p, p, p, p, None, 2, 4, 2, 128, None) == binding.PLX_ERR_INVALID_ARG
+
+
+def test_backward_and_projection_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(4096)
+    bwd = lib.plx_prefill_bwd
+    ptrs = [p] * 13
+    assert bwd(*([None] + ptrs[1:]), 1, 2, 1, 16, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert bwd(*ptrs, 1, 2, 1, 16, 64, None) == binding.PLX_ERR_UNSUPPORTED
+    assert bwd(*ptrs, 1, 3, 2, 16, 128, None) == binding.PLX_ERR_INVALID_ARG
+    mis = ptrs[:8] + [ctypes.c_void_p(4100)] + ptrs[9:]
+    assert bwd(*mis, 1, 2, 1, 16, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert b"aligned" in lib.plx_last_error_message()
+    proj = lib.plx_qkvr_proj
+    assert proj(p, p, p, p, p, p, 1, 16, 100, 2, 1, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert b"multiple of 8" in lib.plx_last_error_message()
+    assert proj(p, p, p, p, p, p, 1, 16, 128, 2, 1, 64, None) == binding.PLX_ERR_UNSUPPORTED
+    assert proj(p, p, None, p, p, p, 1, 16, 128, 2, 1, 128, None) == binding.PLX_ERR_INVALID_ARG
