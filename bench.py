@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # captures summarised in profiles/ (prefill: the bench's own workload;
 # decode: a quarter-size batch scaled by 4, the traffic being proportional to
 # the cache streamed). Set to None whenever a kernel changes after its capture.
-NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": 377.6e6, "decode_split_kernel": 4 * 543.9e6}
+NCU_TRAFFIC_BYTES = {"prefill_tc_kernel": 377.6e6, "decode_split_kernel": 4 * 540.25e6}
 
 
 def load_peaks():
@@ -466,6 +466,23 @@ def main():
             torch.cuda.synchronize(dev)
             return a.elapsed_time(b) / n * 1e-3
 
+        l2_flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+        def launch_cold_s(fn, n):
+            """Mean seconds per call of fn() with L2 flushed before each call
+            (a 512 MB write outside the timed interval), 3 untimed calls first."""
+            for _ in range(3):
+                fn()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for e0, e1 in evs:
+                l2_flush.zero_()
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return sum(e0.elapsed_time(e1) for e0, e1 in evs) / n * 1e-3
+
         def tflops(name, flops, t):
             extra[name] = {"value": flops / t / 1e12, "unit": "TFLOP/s", "ms": t * 1e3,
                            "frac_of_peak": flops / t / 1e12 / tc_peak}
@@ -515,6 +532,32 @@ def main():
             tflops(f"qkvr_projection_{tag}_T{wp.B * wp.L}_D{dm}_F{F}", 2 * wp.B * wp.L * dm * F,
                    launch_s(lambda: plx_qkvr_proj(xt, wt, wp.B, wp.L, wp.Hq, wp.Hkv, wp.d, *po), 10))
             del xt, wt, po
+        # Sweeps (head layout of the 0.6B / 1.7B models: Hq 16, Hkv 8, d 128):
+        # prefill at several context lengths with 16384 tokens per call, and
+        # decode across batch sizes (8192 cached tokens) and contexts (16
+        # sequences), each decode call after an L2 flush (several of these
+        # caches fit in L2).
+        for B_, L_ in ((16, 1024), (8, 2048), (2, 8192), (1, 32768)):
+            qs, ks, vs, rs = inputs.prefill_inputs(B_, 16, 8, L_, 128, torch.bfloat16, 0.05, 2000 + L_,
+                                                   device=dev)
+            os_ = torch.empty_like(qs)
+            fl = 8 * 128 * B_ * 16 * L_ * (L_ + 1) // 2
+            tflops(f"prefill_sweep_B{B_}_L{L_}", fl,
+                   launch_s(lambda: plx_prefill_fwd(qs, ks, vs, rs, os_), 5))
+            del qs, ks, vs, rs, os_
+        for B_, ctx in ((1, 8192), (1, 131072), (4, 8192), (8, 8192), (32, 8192), (128, 8192),
+                        (16, 2048), (16, 32768)):
+            ds = inputs.decode_inputs(B_, 16, 8, 128, [ctx] * B_, torch.bfloat16, 0.05, 3000 + B_,
+                                      device=dev)
+            sls = ds[4].to(dev)
+            ods = torch.empty_like(ds[0])
+            by = 2 * B_ * ctx * 8 * 128 * 2 + 3 * B_ * 16 * 128 * 2
+            td = launch_cold_s(lambda: plx_decode_fwd(ds[0], ds[1], ds[2], ds[3], sls, ods), 10)
+            extra[f"decode_sweep_B{B_}_ctx{ctx}"] = {"value": by / td / 1e9, "unit": "GB/s",
+                                                     "ms": td * 1e3,
+                                                     "frac_of_peak": by / td / 1e9 / hbm_peak,
+                                                     "l2": "flushed before each call"}
+            del ds, sls, ods
         w5 = inputs.DECODE_RAGGED
         d5 = inputs.decode_inputs_for(w5, device=dev)
         sl5 = d5[4].to(dev)

@@ -164,31 +164,45 @@ plx_status plx_prefill_fwd_f32(const float *q, const float *k, const float *v, c
                                void *stream);
 
 /*
- * Decode: one new query per sequence against its KV cache (split-KV + a
- * log-sum-exp combine), bf16 in / out, fp32 accumulation.
+ * Decode: one new query per sequence against its KV cache, bf16 in / out,
+ * fp32 accumulation ("Parallax: parametrized local linear attention for
+ * language modeling", sections "Core mechanism" and "Hardware-aware
+ * algorithm": the covariance branch reads the same key and value stream as
+ * the softmax branch).
  *   q, r           : bf16 [B, Hq, d]
  *   kcache, vcache : bf16 packed [sum_b seqlens[b], Hkv, d]; sequence b starts
- *                    at token sum_{b' < b} seqlens[b']. The cache already holds
- *                    the current token: the query sees all seqlens[b] keys.
+ *                    at token sum_{b' < b} seqlens[b'], fewer than 2^30 tokens
+ *                    in all. The cache already holds the current token: the
+ *                    query sees all seqlens[b] keys.
  *   seqlens        : int32 [B] on the device, each >= 0. A sequence of length
  *                    0 gets an all-zero output row.
  *   out            : bf16 [B, Hq, d]
- *   d must be 128; Hq % Hkv == 0 and Hq / Hkv <= 8. Per-split partial results
- *   go to a stream-ordered scratch buffer (cudaMallocAsync / cudaFreeAsync on
- *   `stream`) sized from B, Hq, d and the split count.
+ *   d must be 128; Hq % Hkv == 0, Hq / Hkv <= 8 and B * Hq <= 2^24.
+ * The keys of all sequences and kv heads form one stream that is cut into
+ * equal shares, one CTA each, so a ragged batch keeps every CTA equally busy;
+ * each CTA writes a partial record (log-sum-exp, normalised O1, O2, sigma)
+ * per (sequence, query head) it meets, and a second kernel combines them.
+ * The records go to a stream-ordered scratch buffer (cudaMallocAsync /
+ * cudaFreeAsync on `stream`) of plx_decode_workspace_bytes(B, Hq, Hkv, d,
+ * plx_decode_default_nsplit(B, Hkv)) bytes.
  */
 plx_status plx_decode_fwd(const void *q, const void *r, const void *kcache, const void *vcache,
                           const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
                           void *stream);
 
 /*
- * plx_decode_fwd with an explicit split count (nsplit >= 1 splits per
- * sequence, keys of split s: [ceil(len*s/nsplit), ceil(len*(s+1)/nsplit)))
- * and a caller-provided device workspace of at least
- * plx_decode_workspace_bytes(B, Hq, d, nsplit) bytes, 16-byte aligned.
- * nsplit <= 0 picks the default; workspace == NULL allocates as
- * plx_decode_fwd does. The result does not depend on nsplit beyond fp32
- * rounding.
+ * plx_decode_fwd with an explicit number of shares, nsplit >= 1 (one CTA
+ * each; share c of n holds the keys [floor(c W / n), floor((c + 1) W / n)) of
+ * the W keys of the batch, sequence-major, then kv head, then token; at most
+ * W shares take part), and a caller-provided device workspace of at least
+ * plx_decode_workspace_bytes(B, Hq, Hkv, d, nsplit) bytes, 16-byte aligned.
+ * nsplit <= 0 picks the default schedule: plx_decode_default_nsplit shares,
+ * fewer for small batches so that every share holds at least 512 keys; when
+ * all sequences of nonzero length have one length, a count that cuts every
+ * (sequence, kv head) row at the same keys or gives every share whole rows,
+ * if that keeps at least 80% of the shares.
+ * workspace == NULL allocates as plx_decode_fwd does. The result does not
+ * depend on nsplit beyond fp32 rounding.
  */
 plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, const void *vcache,
                              const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
@@ -199,7 +213,7 @@ plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, c
  * plx_prefill_fwd_cor for the reading): arguments, layouts, allocation and
  * results as plx_decode_fwd, plus
  *   cor : fp32 [B, Hq], must not be NULL; 0 for sequences of length 0.
- * The ratio is formed after the split records are combined, from the
+ * The ratio is formed after the partial records are combined, from the
  * combined fp32 correction and output.
  */
 plx_status plx_decode_fwd_cor(const void *q, const void *r, const void *kcache, const void *vcache,
@@ -213,12 +227,12 @@ plx_status plx_decode_fwd_cor(const void *q, const void *r, const void *kcache, 
  * allocation locks, or an embedding that gives this library only its own
  * input and output buffers. There is no counterpart in the
  * paper; it exists for such callers only. Same arguments, layouts and results
- * as plx_decode_fwd; the per-split records go to one fixed device array of
+ * as plx_decode_fwd; the partial records go to one fixed device array of
  * 16 MiB that the library reserves on every device that loads it, held until
  * the process exits. Nothing is allocated or freed by this call.
- *   - The split count is the default one, lowered if needed so the records
- *     fit; B * Hq * (2 d + 2) * 4 bytes (one split) must fit in 16 MiB, else
- *     PLX_ERR_UNSUPPORTED and nothing runs.
+ *   - The schedule is the default one, with fewer shares if needed so the
+ *     records fit; plx_decode_workspace_bytes(B, Hq, Hkv, d, 1) must fit in
+ *     16 MiB, else PLX_ERR_UNSUPPORTED and nothing runs.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  *   - Every call shares the array: calls that overlap on the GPU race and must
@@ -229,18 +243,23 @@ plx_status plx_decode_fwd_noalloc(const void *q, const void *r, const void *kcac
                                   const void *vcache, const int *seqlens, void *out, int B, int Hq,
                                   int Hkv, int d, void *stream);
 
-/* Bytes of decode workspace for a given split count (fp32 partials:
- * B * Hq * nsplit * (2 d + 2) * 4). */
-size_t plx_decode_workspace_bytes(int B, int Hq, int d, int nsplit);
+/* Bytes of decode workspace for nsplit shares: a table of 8 bytes per
+ * (sequence, kv head) rounded up to 256 bytes, then
+ * (nsplit * Hq / Hkv + B * Hq) fp32 records of 2 d + 2 floats. 0 for
+ * arguments out of range. */
+size_t plx_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int nsplit);
 
-/* The split count plx_decode_fwd uses on the current device for B sequences
- * of Hkv KV heads: about 12 CTAs per SM in total, at most 256 splits
- * (lengths are on the device, so the host does not look at them). */
+/* The number of shares plx_decode_fwd starts from on the current device: two
+ * CTAs per SM, one wave of the split kernel (B and Hkv do not change it; the
+ * kernel itself uses fewer for small batches, since lengths are on the device). */
 int plx_decode_default_nsplit(int B, int Hkv);
 
 /* Synchronises `stream`, then reads and clears the device error word.
  * PLX_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the last check,
- * PLX_ERR_CUDA if the stream reports an error, else PLX_OK. */
+ * PLX_ERR_INVALID_ARG if a kernel found its device-side inputs out of range
+ * (decode lengths summing to 2^30 tokens or more; that call did no work and
+ * its outputs are undefined), PLX_ERR_CUDA if the stream reports an error,
+ * else PLX_OK. */
 plx_status plx_check_device_error(void *stream);
 
 /* Launches one block whose wait on an mbarrier that nothing ever arrives on

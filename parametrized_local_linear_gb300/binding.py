@@ -38,7 +38,7 @@ SIGNATURES = {
     "plx_decode_fwd_ex": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _sz, _vp]),
     "plx_decode_fwd_noalloc": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
     "plx_decode_fwd_cor": (_i, [_vp] * 7 + [_i] * 4 + [_vp]),
-    "plx_decode_workspace_bytes": (_sz, [_i] * 4),
+    "plx_decode_workspace_bytes": (_sz, [_i] * 5),
     "plx_decode_default_nsplit": (_i, [_i] * 2),
     "plx_check_device_error": (_i, [_vp]),
     "plx_debug_timeout_probe": (_i, [_ll, _vp]),
@@ -327,7 +327,7 @@ def plx_decode_fwd(q, r, kcache, vcache, seqlens, out=None, nsplit=0, workspace=
 
 def plx_decode_fwd_noalloc(q, r, kcache, vcache, seqlens, out, stream=None):
     """Decode through the entry point that allocates nothing (see include/plx.h):
-    the split records go to the library's fixed device array. ``out`` must be
+    the partial records go to the library's fixed device array. ``out`` must be
     given (bf16 [B, Hq, d]); returns it."""
     _need(q, "q", torch.bfloat16, 3)
     dev = q.device
@@ -374,8 +374,8 @@ def plx_decode_fwd_cor(q, r, kcache, vcache, seqlens, out=None, cor=None, stream
     return out, cor
 
 
-def plx_decode_workspace_bytes(B, Hq, d, nsplit) -> int:
-    return int(lib().plx_decode_workspace_bytes(B, Hq, d, nsplit))
+def plx_decode_workspace_bytes(B, Hq, Hkv, d, nsplit) -> int:
+    return int(lib().plx_decode_workspace_bytes(B, Hq, Hkv, d, nsplit))
 
 
 def plx_decode_default_nsplit(B, Hkv) -> int:

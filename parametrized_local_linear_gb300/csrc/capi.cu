@@ -7,6 +7,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/plx.h"
@@ -250,46 +251,44 @@ plx_status plx_qkvr_proj(const void *x, const void *w, void *q, void *k, void *v
                        fn);
 }
 
-size_t plx_decode_workspace_bytes(int B, int Hq, int d, int nsplit) {
-  if (B < 1 || Hq < 1 || d < 1 || nsplit < 1) return 0;
-  return static_cast<size_t>(B) * Hq * nsplit * (2 * static_cast<size_t>(d) + 2) * sizeof(float);
+size_t plx_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int nsplit) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || nsplit < 1 || Hq % Hkv != 0) return 0;
+  return plx::decode_workspace_bytes(B, Hq, Hkv, d, nsplit);
 }
 
 int plx_decode_default_nsplit(int B, int Hkv) {
-  if (B < 1 || Hkv < 1) return 1;
-  // Lengths live on the device, so the split count cannot look at them. Aim
-  // for about 12 CTAs per SM in total (6 waves of 2 resident CTAs): enough
-  // splits to even out a ragged batch, few enough that each CTA streams a
-  // long run of keys. Measured on GB300, batched decode (B=64, 8192 tokens):
-  // 10 splits 6.06 TB/s, 4 splits 6.70; ragged (B=8, 16k-131k): 76 splits
-  // 5.88, 32 splits 6.56.
-  const long long target = 12LL * plx::sm_count();
-  long long n = (target + static_cast<long long>(B) * Hkv - 1) / (static_cast<long long>(B) * Hkv);
-  if (n < 1) n = 1;
-  if (n > 256) n = 256;
-  return static_cast<int>(n);
+  (void)B;
+  (void)Hkv;
+  // One wave of the split kernel: two CTAs fit on an SM (its registers), and
+  // every CTA takes an equal share of the batch's keys, so a single wave keeps
+  // every SM streaming until the end with no tail. Lengths live on the
+  // device, so the kernel itself lowers the count for small batches (at least
+  // 512 keys a CTA). Measured on GB300 with per-sequence splits before this
+  // schedule: uniform batches ran fastest at 256 CTAs (B = 1..32, 8192
+  // tokens), a ragged one (B = 8, 16k-131k tokens) needed 32 splits a
+  // sequence to even out its lengths.
+  return 2 * plx::sm_count();
 }
 
 namespace {
 
 plx_status decode_bf16(const char *fn, const void *q, const void *r, const void *kcache,
                        const void *vcache, const int *seqlens, void *out, float *cor, int B,
-                       int Hq, int Hkv, int d, int nsplit, void *workspace, size_t workspace_bytes,
-                       void *stream) {
+                       int Hq, int Hkv, int d, int nsplit, bool default_share, void *workspace,
+                       size_t workspace_bytes, void *stream) {
   if (!q || !r || !kcache || !vcache || !seqlens || !out)
     return fail(PLX_ERR_INVALID_ARG, "%s: null pointer", fn);
   plx_status s = check_common(fn, B, Hq, Hkv, 1, d);
   if (s) return s;
   if (d != 128) return fail(PLX_ERR_UNSUPPORTED, "%s: head dim %d (only 128)", fn, d);
   if (Hq / Hkv > 8) return fail(PLX_ERR_UNSUPPORTED, "%s: Hq / Hkv = %d (at most 8)", fn, Hq / Hkv);
-  if (B > 65535 || Hkv > 65535) return fail(PLX_ERR_UNSUPPORTED, "%s: B and Hkv must be <= 65535", fn);
+  if (static_cast<long long>(B) * Hq > (1LL << 24))
+    return fail(PLX_ERR_UNSUPPORTED, "%s: B * Hq must be <= 2^24", fn);
   if (!aligned16(q) || !aligned16(r) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
     return fail(PLX_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", fn);
-  if (nsplit <= 0) nsplit = plx_decode_default_nsplit(B, Hkv);
+  if (nsplit < 1) return fail(PLX_ERR_INVALID_ARG, "%s: nsplit %d", fn, nsplit);
   if (nsplit > 65535) return fail(PLX_ERR_INVALID_ARG, "%s: nsplit %d too large", fn, nsplit);
-  if (static_cast<long long>(B) * Hkv * nsplit > 0x7fffffffLL)
-    return fail(PLX_ERR_UNSUPPORTED, "%s: B * Hkv * nsplit exceeds 2^31 - 1", fn);
-  const size_t need = plx_decode_workspace_bytes(B, Hq, d, nsplit);
+  const size_t need = plx::decode_workspace_bytes(B, Hq, Hkv, d, nsplit);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (workspace != nullptr) {
     if (workspace_bytes < need)
@@ -297,7 +296,7 @@ plx_status decode_bf16(const char *fn, const void *q, const void *r, const void 
                   need);
     if (!aligned16(workspace)) return fail(PLX_ERR_INVALID_ARG, "%s: workspace not 16-byte aligned", fn);
     return finish_launch(plx::launch_decode(q, r, kcache, vcache, seqlens, out, cor, B, Hq, Hkv,
-                                            nsplit, static_cast<float *>(workspace),
+                                            nsplit, default_share, workspace,
                                             plx::device_error_word(), st),
                          fn);
   }
@@ -305,7 +304,7 @@ plx_status decode_bf16(const char *fn, const void *q, const void *r, const void 
   cudaError_t e = cudaMallocAsync(&ws, need, st);
   if (e != cudaSuccess) return cuda_fail(e, "plx_decode_fwd: workspace allocation");
   e = plx::launch_decode(q, r, kcache, vcache, seqlens, out, cor, B, Hq, Hkv, nsplit,
-                         static_cast<float *>(ws), plx::device_error_word(), st);
+                         default_share, ws, plx::device_error_word(), st);
   cudaError_t e2 = cudaFreeAsync(ws, st);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   if (e2 != cudaSuccess) return cuda_fail(e2, "plx_decode_fwd: workspace release");
@@ -317,8 +316,10 @@ plx_status decode_bf16(const char *fn, const void *q, const void *r, const void 
 plx_status plx_decode_fwd_ex(const void *q, const void *r, const void *kcache, const void *vcache,
                              const int *seqlens, void *out, int B, int Hq, int Hkv, int d,
                              int nsplit, void *workspace, size_t workspace_bytes, void *stream) {
+  const bool default_share = nsplit <= 0;
   return decode_bf16("plx_decode_fwd", q, r, kcache, vcache, seqlens, out, nullptr, B, Hq, Hkv, d,
-                     nsplit, workspace, workspace_bytes, stream);
+                     default_share ? plx_decode_default_nsplit(B, Hkv) : nsplit, default_share,
+                     workspace, workspace_bytes, stream);
 }
 
 plx_status plx_decode_fwd_cor(const void *q, const void *r, const void *kcache, const void *vcache,
@@ -326,7 +327,7 @@ plx_status plx_decode_fwd_cor(const void *q, const void *r, const void *kcache, 
                               int d, void *stream) {
   if (!cor) return fail(PLX_ERR_INVALID_ARG, "plx_decode_fwd_cor: null cor pointer");
   return decode_bf16("plx_decode_fwd_cor", q, r, kcache, vcache, seqlens, out, cor, B, Hq, Hkv, d,
-                     0, nullptr, 0, stream);
+                     plx_decode_default_nsplit(B, Hkv), true, nullptr, 0, stream);
 }
 
 plx_status plx_decode_fwd(const void *q, const void *r, const void *kcache, const void *vcache,
@@ -341,22 +342,27 @@ plx_status plx_decode_fwd_noalloc(const void *q, const void *r, const void *kcac
                                   int Hkv, int d, void *stream) {
   const char *fn = "plx_decode_fwd_noalloc";
   const size_t cap_bytes = plx::kNoAllocScratchFloats * sizeof(float);
-  int nsplit = plx_decode_default_nsplit(B, Hkv);
-  if (B >= 1 && Hq >= 1 && d >= 1) {
-    const size_t per_split = plx_decode_workspace_bytes(B, Hq, d, 1);
-    if (per_split > cap_bytes)
+  if (B >= 1 && Hq >= 1 && Hkv >= 1 && d >= 1 && Hq % Hkv == 0) {
+    const size_t one = plx_decode_workspace_bytes(B, Hq, Hkv, d, 1);
+    if (one > cap_bytes)
       return fail(PLX_ERR_UNSUPPORTED,
-                  "%s: B * Hq = %lld needs %zu bytes of split records even with one split; "
+                  "%s: B * Hq = %lld needs %zu bytes of records even with one CTA; "
                   "the fixed array holds %zu bytes (use plx_decode_fwd)",
-                  fn, static_cast<long long>(B) * Hq, per_split, cap_bytes);
-    const size_t fit = cap_bytes / per_split;
-    if (static_cast<size_t>(nsplit) > fit) nsplit = static_cast<int>(fit);
+                  fn, static_cast<long long>(B) * Hq, one, cap_bytes);
   }
   float *scratch = nullptr;
   cudaError_t e = plx::noalloc_scratch(&scratch);
   if (e != cudaSuccess) return cuda_fail(e, "plx_decode_fwd_noalloc: scratch address");
-  return plx_decode_fwd_ex(q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, d, nsplit, scratch,
-                           cap_bytes, stream);
+  // The default schedule, with as many CTAs as the array has records for.
+  int nshare = plx_decode_default_nsplit(B, Hkv);
+  while (nshare > 1 && plx_decode_workspace_bytes(B, Hq, Hkv, d, nshare) > cap_bytes) {
+    const size_t per = plx_decode_workspace_bytes(B, Hq, Hkv, d, 2) -
+                       plx_decode_workspace_bytes(B, Hq, Hkv, d, 1);
+    const size_t over = plx_decode_workspace_bytes(B, Hq, Hkv, d, nshare) - cap_bytes;
+    nshare -= static_cast<int>(std::min<size_t>(nshare - 1, (over + per - 1) / per));
+  }
+  return decode_bf16(fn, q, r, kcache, vcache, seqlens, out, nullptr, B, Hq, Hkv, d, nshare, true,
+                     scratch, cap_bytes, stream);
 }
 
 plx_status plx_check_device_error(void *stream) {
@@ -372,6 +378,11 @@ plx_status plx_check_device_error(void *stream) {
   if (e != cudaSuccess) return cuda_fail(e, "plx_check_device_error: read");
   if (v & plx::kErrTimeout)
     return fail(PLX_ERR_DEVICE_TIMEOUT, "a bounded in-kernel wait ran out (error word 0x%x)", v);
+  if (v & plx::kErrBadInput)
+    return fail(PLX_ERR_INVALID_ARG,
+                "a kernel found device-side inputs out of range (decode: seqlens sum to 2^30 "
+                "tokens or more); its outputs are undefined (error word 0x%x)",
+                v);
   return PLX_OK;
 }
 

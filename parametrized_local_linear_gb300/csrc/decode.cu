@@ -43,6 +43,7 @@ namespace {
 constexpr int D = 128;
 constexpr int KT = 16;                        // keys per stage (one TMA box row count)
 constexpr int NCW = 4;                        // consumer warps
+constexpr int GMAX = 8;                       // query heads per kv head (A rows 0..7 and 8..15)
 // Tile t goes to warp t % NCW and stage t % NST. NST is a multiple of NCW, so
 // a stage is only ever consumed by one warp, which has itself consumed the
 // stage's previous phase before it waits on the next one: a parity wait can
@@ -50,19 +51,42 @@ constexpr int NCW = 4;                        // consumer warps
 constexpr int NST = 2 * NCW;                  // stages in the ring
 constexpr int HALF = KT * 128;                // one 64-dim half of KT rows, 128-byte swizzled
 constexpr int STAGE_BYTES = 4 * HALF;         // K half 0, K half 1, V half 0, V half 1
-constexpr int OFF_BAR = NST * STAGE_BYTES;    // 65536
+constexpr int OFF_RED = NST * STAGE_BYTES;    // 65536: per-warp partials of one item
+constexpr int RED_FLOATS = NCW * 2 * GMAX * D;
+constexpr int OFF_MLS = OFF_RED + RED_FLOATS * 4;
+constexpr int MLS_FLOATS = NCW * GMAX * 3;
+constexpr int OFF_BAR = OFF_MLS + MLS_FLOATS * 4;
+constexpr int OFF_FLAG = OFF_BAR + 2 * NST * 8;
+constexpr int OFF_PLAN = OFF_FLAG + 16;
 static_assert(NST % NCW == 0, "each stage must belong to one consumer warp");
-constexpr int SMEM_BYTES = OFF_BAR + 2 * NST * 8 + 16 + 1024;  // + alignment slack
+static_assert(OFF_BAR % 8 == 0 && OFF_PLAN % 16 == 0, "barrier and plan alignment");
+constexpr int SMEM_BYTES = OFF_PLAN + 64 + 1024;  // + alignment slack
 constexpr int REC = 2 * D + 2;                // floats per partial record
 constexpr int THREADS = 32 * (NCW + 1);
+// Fewest keys the default schedule gives one CTA: below about 512 keys the
+// fixed cost of a CTA (tensor-map prefetch, pipeline fill, the merge) is no
+// longer small against its stream, and small batches ran fastest on GB300
+// with 128 to 256 CTAs of 256 to 1024 keys each.
+constexpr int kDefaultMinKeys = 512;
 
 struct DecodeArgs {
   const __nv_bfloat16 *q, *r;
   const int *seqlens;
-  float *ws;
-  int B, Hq, Hkv, G, nsplit;
+  float *recs;  // [(nshare * G + B * Hq)][REC] partial records
+  int2 *meta;   // [B * Hkv] {first record slot, number of slots} of each (sequence, kv head)
+  int B, Hq, Hkv, G, nshare, min_keys;
+  bool align;        // default schedule: align the shares with the rows of a uniform batch
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned *err;
+};
+
+// The CTA's share of the batch, worked out once by the producer warp.
+struct Plan {
+  long long W;      // keys of the whole batch over all kv heads
+  long long s, e;   // this CTA's share [s, e) of the flattened key stream
+  long long pb0;    // first token of sequence b0
+  int n;            // CTAs with work (n <= gridDim.x)
+  int b0;           // the sequence holding position s; -1: no work
 };
 
 // Byte offset of 16-byte chunk c (0..15 over the 128 dims) of row `row` in a
@@ -70,6 +94,48 @@ struct DecodeArgs {
 __device__ __forceinline__ uint32_t swz(int row, int c) {
   return (c >> 3) * HALF + row * 128 + ((((c & 7) ^ (row & 7))) << 4);
 }
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
+}
+
+// The batch is one flattened stream of keys: sequence b's kv head h holds the
+// positions [Hkv P_b + h len_b, Hkv P_b + (h + 1) len_b), P_b the tokens in
+// front of sequence b. CTA c of n takes [floor(c W / n), floor((c + 1) W / n))
+// and cuts it at the (sequence, kv head) boundaries into items. Every warp
+// walks the same items from the plan, so they agree on every item without
+// talking to each other.
+struct Item {
+  int b, kvh, k0, k1;  // keys [k0, k1) of kv head kvh of sequence b
+  int len;             // keys of sequence b
+  long long tok0;      // first token of sequence b in the cache
+};
+
+struct Walk {
+  long long pos, e, pb, row_base;
+  int b, len;
+  __device__ __forceinline__ Walk(const Plan &p, const int *seqlens, int Hkv)
+      : pos(p.s), e(p.e), pb(p.pb0), row_base(p.pb0 * Hkv), b(p.b0),
+        len(max(seqlens[p.b0], 0)) {}
+  __device__ __forceinline__ bool next(Item &it, const int *seqlens, int Hkv) {
+    if (pos >= e) return false;
+    // Positions below W all lie in some sequence, so b stays below B here.
+    while (pos >= row_base + static_cast<long long>(Hkv) * len) {
+      pb += len;
+      row_base = pb * Hkv;
+      len = max(seqlens[++b], 0);
+    }
+    const long long off = pos - row_base;
+    it.b = b;
+    it.kvh = static_cast<int>(off / len);
+    it.k0 = static_cast<int>(off - static_cast<long long>(it.kvh) * len);
+    it.k1 = static_cast<int>(min(static_cast<long long>(len), it.k0 + (e - pos)));
+    it.len = len;
+    it.tok0 = pb;
+    pos += it.k1 - it.k0;
+    return true;
+  }
+};
 
 __global__ void __launch_bounds__(THREADS)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -79,80 +145,170 @@ __global__ void __launch_bounds__(THREADS)
                                               ~static_cast<uintptr_t>(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *empty = full + NST;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + NST);
-
-  // kv heads vary fastest across the grid, so the CTAs that run side by side
-  // read the same token range of neighbouring heads (adjacent 256-byte rows
-  // of the cache): +1.5% on the ragged batch.
-  const int kvh = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_FLAG);
+  Plan *plan = reinterpret_cast<Plan *>(smem + OFF_PLAN);
+  const int c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int len = a.seqlens[b];
-  const int lo = static_cast<int>((static_cast<long long>(len) * split + a.nsplit - 1) / a.nsplit);
-  const int hi =
-      static_cast<int>((static_cast<long long>(len) * (split + 1) + a.nsplit - 1) / a.nsplit);
-  const int nkeys = hi - lo;
-  const int ntiles = (nkeys + KT - 1) / KT;
 
+  if (warp == NCW) {
+    // ------------------------------------------------------------ plan
+    long long T = 0;
+    int nz = 0, lmin = 0x7fffffff, lmax = 0;  // over the sequences of nonzero length
+#pragma unroll 4
+    for (int i = lane; i < a.B; i += 32) {
+      const int len = max(a.seqlens[i], 0);
+      T += len;
+      if (len > 0) {
+        ++nz;
+        lmin = min(lmin, len);
+        lmax = max(lmax, len);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      T += __shfl_xor_sync(0xffffffffu, T, o);
+      nz += __shfl_xor_sync(0xffffffffu, nz, o);
+      lmin = min(lmin, __shfl_xor_sync(0xffffffffu, lmin, o));
+      lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+    }
+    if (T >= (1LL << 30)) {  // past the tensor maps' token extent: no work
+      if (lane == 0 && c == 0 && a.err) atomicOr(a.err, kErrBadInput);
+      T = 0;
+      nz = 0;
+    }
+    const long long W = T * a.Hkv;
+    long long n = (W + a.min_keys - 1) / a.min_keys;
+    n = max(1LL, min(static_cast<long long>(a.nshare), n));
+    if (a.align && nz > 0 && lmin == lmax) {
+      // Rows of one length: cut every row at the same keys (k shares a row)
+      // or give every share whole rows (m rows a share), so that the CTAs
+      // streaming the kv heads of a sequence read the same tokens at the
+      // same time (neighbouring 256-byte rows of the cache). Measured on
+      // GB300 (B = 64, 8192 tokens): 256 aligned shares 6.58 TB/s, 304
+      // unaligned 6.34. Taken only if it keeps 80% of the CTAs.
+      const long long R = static_cast<long long>(nz) * a.Hkv, floor_n = (4 * n + 4) / 5;
+      long long best = 0;
+      if (R <= n) {
+        best = R * (n / R);
+      } else {
+        for (long long m = (R + n - 1) / n, m_end = m + 64; m < m_end && R / m >= floor_n; ++m)
+          if (R % m == 0) {
+            best = R / m;
+            break;
+          }
+      }
+      if (best >= floor_n) n = best;
+    }
+    const long long s = c * W / n, e = (c + 1) * W / n;
+    int b0 = -1;
+    long long pb0 = 0;
+    if (c < n && s < e) {
+      // The first sequence whose flattened end lies past s.
+      long long base = 0;
+      for (int i0 = 0; i0 < a.B; i0 += 32) {
+        const int i = i0 + lane;
+        const long long len = i < a.B ? max(a.seqlens[i], 0) : 0;
+        long long inc = len;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const long long v = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += v;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, i < a.B && (base + inc) * a.Hkv > s);
+        if (hit != 0u) {
+          const int l = __ffs(hit) - 1;
+          b0 = i0 + l;
+          pb0 = base + __shfl_sync(0xffffffffu, inc - len, l);
+          break;
+        }
+        base += __shfl_sync(0xffffffffu, inc, 31);
+      }
+    }
+    if (lane == 0) {
+      plan->W = W;
+      plan->s = s;
+      plan->e = e;
+      plan->pb0 = pb0;
+      plan->n = static_cast<int>(n);
+      plan->b0 = b0;
+    }
+  }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(smem_u32(&full[st]), 1);
+      mbar_init(smem_u32(&empty[st]), 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
+  const Plan pl = *plan;
+  if (pl.b0 < 0) return;  // no share: more CTAs than the batch needs
   const Abort ab{abort_flag, a.err};
 
-  // Tile t covers keys [lo + KT t, min(lo + KT (t + 1), hi)). Its TMA box of KT
-  // tokens starts at token min(off + lo + KT t, off + hi - KT), so the box
-  // never reaches past the split's last key (and so never past the cache);
-  // rows in front of the tile's first key (`skip` of them: keys of the
-  // previous tile, or zero fill before token 0) are masked by the consumer.
+  // Tile t of an item covers keys [k0 + KT t, min(k0 + KT (t + 1), k1)). Its
+  // TMA box of KT tokens starts at token min(tok0 + k0 + KT t, tok0 + k1 - KT),
+  // so the box never reaches past the item's last key (and so never past the
+  // cache); rows in front of the tile's first key (`skip` of them: keys of the
+  // previous tile, of another sequence, or zero fill before token 0) are
+  // masked by the consumer. Tiles are numbered across the CTA's items (g), so
+  // stages and parities run on from one item to the next.
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
-    long long off = 0;
-    for (int i = lane; i < b; i += 32) off += a.seqlens[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
     if (lane == 0) {
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      const int first = static_cast<int>(off) + lo, last = static_cast<int>(off) + hi;
-      int issued = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t % NST;
-        if (t >= NST && !mbar_wait(smem_u32(&empty[st]), ((t / NST) - 1) & 1, ab)) break;
-        const uint32_t bar = smem_u32(&full[st]);
-        mbar_arrive_expect_tx(bar, STAGE_BYTES);
-        const int z = min(first + KT * t, last - KT);
-        const uint32_t base = smem_u32(smem + st * STAGE_BYTES);
-        tma_load_3d(base, &tm_k, 0, kvh, z, bar);
-        tma_load_3d(base + HALF, &tm_k, 64, kvh, z, bar);
-        tma_load_3d(base + 2 * HALF, &tm_v, 0, kvh, z, bar);
-        tma_load_3d(base + 3 * HALF, &tm_v, 64, kvh, z, bar);
-        issued = t + 1;
+      Walk wk(pl, a.seqlens, a.Hkv);
+      Item it;
+      int g = 0;
+      bool ok = true;
+      while (ok && wk.next(it, a.seqlens, a.Hkv)) {
+        const int first = static_cast<int>(it.tok0) + it.k0, last = static_cast<int>(it.tok0) + it.k1;
+        const int nt = (it.k1 - it.k0 + KT - 1) / KT;
+        for (int t = 0; t < nt; ++t, ++g) {
+          const int st = g % NST;
+          if (g >= NST && !mbar_wait(smem_u32(&empty[st]), ((g / NST) - 1) & 1, ab)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&full[st]);
+          mbar_arrive_expect_tx(bar, STAGE_BYTES);
+          const int z = min(first + KT * t, last - KT);
+          const uint32_t base = smem_u32(smem + st * STAGE_BYTES);
+          tma_load_3d(base, &tm_k, 0, it.kvh, z, bar);
+          tma_load_3d(base + HALF, &tm_k, 64, it.kvh, z, bar);
+          tma_load_3d(base + 2 * HALF, &tm_v, 0, it.kvh, z, bar);
+          tma_load_3d(base + 3 * HALF, &tm_v, 64, it.kvh, z, bar);
+        }
       }
-      if (ab.raised()) {
-        // Let this thread's own copies land before the CTA exits.
-        for (int t = max(0, issued - NST); t < issued; ++t)
+      if (!ok) {
+        // Let this thread's own copies (tiles g - NST .. g - 1) land before the CTA exits.
+        for (int t = max(0, g - NST); t < g; ++t)
           mbar_wait_drain(smem_u32(&full[t % NST]), (t / NST) & 1);
       }
     }
+    return;
   }
 
   // ------------------------------------------------------------ consumers
+  // Every consumer warp takes part in every item's merge (both barriers),
+  // also after an abort, so the named barrier is always complete.
   const int g = lane >> 2, tq = lane & 3;
-  float acc[16][4];
-  float m = -INFINITY, l = 0.f, sg = 0.f;
+  float *red = reinterpret_cast<float *>(smem + OFF_RED);  // [NCW][2G][D]
+  float *mls = reinterpret_cast<float *>(smem + OFF_MLS);  // [NCW][G][3]
+  Walk wk(pl, a.seqlens, a.Hkv);
+  Item it;
+  int gt = 0;  // tiles of the previous items
+  while (wk.next(it, a.seqlens, a.Hkv)) {
+    const int nt = (it.k1 - it.k0 + KT - 1) / KT;
+    float acc[16][4];
+    float m = -INFINITY, l = 0.f, sg = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-  if (warp < NCW) {
+    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     uint32_t qa[8][4];
     {
       const bool live = g < a.G;
-      const size_t hrow = (static_cast<size_t>(b) * a.Hq + kvh * a.G + (live ? g : 0)) * D;
+      const size_t hrow = (static_cast<size_t>(it.b) * a.Hq + it.kvh * a.G + (live ? g : 0)) * D;
       const uint32_t *qr = reinterpret_cast<const uint32_t *>(a.q + hrow);
       const uint32_t *rr = reinterpret_cast<const uint32_t *>(a.r + hrow);
 #pragma unroll
@@ -163,28 +319,29 @@ __global__ void __launch_bounds__(THREADS)
         qa[kk][3] = live ? rr[8 * kk + 4 + tq] : 0u;
       }
     }
-    for (int t = warp; t < ntiles; t += NCW) {
-      const int st = t % NST;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(smem_u32(&full[st]), (t / NST) & 1, ab);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    for (int t = (warp - gt % NCW + NCW) % NCW; t < nt; t += NCW) {
+      const int gi = gt + t;
+      const int st = gi % NST;
+      bool ok = false;
+      if (lane == 0) ok = !ab.raised() && mbar_wait(smem_u32(&full[st]), (gi / NST) & 1, ab);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) continue;  // aborting: skip the tile
       const uint32_t kb = smem_u32(smem + st * STAGE_BYTES);
       const uint32_t vb = kb + 2 * HALF;
       // Rows [0, skip) of the box precede this tile's first key.
-      const int skip = (lo + KT * t) - min(lo + KT * t, hi - KT);
+      const int skip = (it.k0 + KT * t) - min(it.k0 + KT * t, it.k1 - KT);
 #pragma unroll
       for (int half = 0; half < KT / 16; ++half) {
         if (half * 16 + 15 < skip) continue;
-        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float cc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int krow = half * 16 + (lane >> 4) * 8 + (lane & 7);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + swz(krow, 2 * kk + ((lane >> 3) & 1)), b0, b1, b2, b3);
-          mma_bf16_16816(c[0], qa[kk], b0, b1);
-          mma_bf16_16816(c[1], qa[kk], b2, b3);
+          mma_bf16_16816(cc[0], qa[kk], b0, b1);
+          mma_bf16_16816(cc[1], qa[kk], b2, b3);
         }
-        // c[n][0..1]: s for box rows half*16 + 8n + 2tq + {0,1}; c[n][2..3]: t for the same rows.
+        // cc[n][0..1]: s for box rows half*16 + 8n + 2tq + {0,1}; cc[n][2..3]: t for the same rows.
         float s[2][2];
         float mx = -INFINITY;
 #pragma unroll
@@ -192,7 +349,7 @@ __global__ void __launch_bounds__(THREADS)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int row = half * 16 + 8 * n + 2 * tq + e;
-            s[n][e] = row >= skip ? c[n][e] * a.scale_log2 : -INFINITY;
+            s[n][e] = row >= skip ? cc[n][e] * a.scale_log2 : -INFINITY;
             mx = fmaxf(mx, s[n][e]);
           }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -206,7 +363,7 @@ __global__ void __launch_bounds__(THREADS)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             p[n][e] = fast_exp2(s[n][e] - msub);
-            pt[n][e] = p[n][e] * c[n][2 + e];
+            pt[n][e] = p[n][e] * cc[n][2 + e];
             ps += p[n][e];
             pts += pt[n][e];
           }
@@ -233,41 +390,39 @@ __global__ void __launch_bounds__(THREADS)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
     }
+    gt += nt;
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
     sg += __shfl_xor_sync(0xffffffffu, sg, 1);
     sg += __shfl_xor_sync(0xffffffffu, sg, 2);
-  }
 
-  // ------------------------------------------------------------ merge warps
-  __syncthreads();  // every stage is consumed (or the CTA aborted): reuse them
-  float *red = reinterpret_cast<float *>(smem);          // [NCW][2G][D]
-  float *mls = red + NCW * 2 * a.G * D;                   // [NCW][G][3]
-  if (warp < NCW && g < a.G) {
-    float *o1 = red + (warp * 2 * a.G + g) * D;
-    float *o2 = red + (warp * 2 * a.G + a.G + g) * D;
+    // ---------------------------------------------------------- merge warps
+    if (g < a.G) {
+      float *o1 = red + (warp * 2 * a.G + g) * D;
+      float *o2 = red + (warp * 2 * a.G + a.G + g) * D;
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      o1[8 * nd + 2 * tq] = acc[nd][0];
-      o1[8 * nd + 2 * tq + 1] = acc[nd][1];
-      o2[8 * nd + 2 * tq] = acc[nd][2];
-      o2[8 * nd + 2 * tq + 1] = acc[nd][3];
+      for (int nd = 0; nd < 16; ++nd) {
+        o1[8 * nd + 2 * tq] = acc[nd][0];
+        o1[8 * nd + 2 * tq + 1] = acc[nd][1];
+        o2[8 * nd + 2 * tq] = acc[nd][2];
+        o2[8 * nd + 2 * tq + 1] = acc[nd][3];
+      }
+      if (tq == 0) {
+        mls[(warp * a.G + g) * 3 + 0] = m;
+        mls[(warp * a.G + g) * 3 + 1] = l;
+        mls[(warp * a.G + g) * 3 + 2] = sg;
+      }
     }
-    if (tq == 0) {
-      mls[(warp * a.G + g) * 3 + 0] = m;
-      mls[(warp * a.G + g) * 3 + 1] = l;
-      mls[(warp * a.G + g) * 3 + 2] = sg;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < D) {
+    consumer_sync();
+    const int row = it.b * a.Hkv + it.kvh;
     const int dim = threadIdx.x;
+    const bool aborted = ab.raised();
     for (int gh = 0; gh < a.G; ++gh) {
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NCW; ++w) M = fmaxf(M, mls[(w * a.G + gh) * 3]);
-      float *rec = a.ws + ((static_cast<size_t>(b) * a.Hq + kvh * a.G + gh) * a.nsplit + split) * REC;
-      if (M == -INFINITY || ab.raised()) {
+      float *rec = a.recs + (static_cast<size_t>(c + row) * a.G + gh) * REC;
+      if (M == -INFINITY || aborted) {
         rec[dim] = 0.f;
         rec[D + dim] = 0.f;
         if (dim == 0) {
@@ -293,34 +448,90 @@ __global__ void __launch_bounds__(THREADS)
         rec[2 * D + 1] = M + log2f(L);
       }
     }
+    if (it.k0 == 0 && dim == 0) {
+      // This CTA holds the row's first key, so it is the first of the CTAs
+      // that hold the row (CTA c' writes its records to slot c' + row); the
+      // last one holds the row's last key x, CTA floor(((x + 1) n - 1) / W).
+      const long long x_last = (it.tok0 * a.Hkv + static_cast<long long>(it.kvh) * it.len) +
+                               it.len - 1;
+      const int c_last = static_cast<int>(((x_last + 1) * pl.n - 1) / pl.W);
+      a.meta[row] = make_int2(c + row, c_last - c + 1);
+    }
+    consumer_sync();  // the next item's partials overwrite red and mls
   }
 }
 
-// One block of D threads per (sequence, query head): merge the splits.
-__global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ ws,
+// One block of D threads per (sequence, query head): merge the row's records.
+// They are read in parallel: each thread takes a strided share of the records'
+// log-sum-exps for the maximum and the weights (staged in shared memory, CCH
+// records at a time), then every thread accumulates its own dimension over
+// the staged records with independent loads in flight.
+constexpr int CCH = 512;
+
+__device__ __forceinline__ float block_max(float v, float *slot) {
+#pragma unroll
+  for (int sh = 16; sh > 0; sh >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, sh));
+  if ((threadIdx.x & 31) == 0) slot[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = slot[0];
+#pragma unroll
+  for (int w = 1; w < D / 32; ++w) v = fmaxf(v, slot[w]);
+  return v;
+}
+
+__global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restrict__ recs,
+                                                          const int2 *__restrict__ meta,
+                                                          const int *__restrict__ seqlens,
                                                           __nv_bfloat16 *__restrict__ out,
-                                                          float *__restrict__ cor, int nsplit) {
+                                                          float *__restrict__ cor, int Hq,
+                                                          int Hkv, int nslots) {
+  __shared__ float wsig[2][CCH];
+  __shared__ float slot[D / 32];
   const int bh = blockIdx.x, dim = threadIdx.x;
-  const float *rec = ws + static_cast<size_t>(bh) * nsplit * REC;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, rec[s * REC + 2 * D + 1]);
+  const int b = bh / Hq, h = bh - b * Hq, G = Hq / Hkv;
+  const int kvh = h / G, gh = h - kvh * G;
   float o = 0.f, c = 0.f;
-  if (M != -INFINITY) {
-    float W = 0.f, o1 = 0.f, o2 = 0.f, sf = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float lse = rec[s * REC + 2 * D + 1];
-      const float w = exp2f(lse - M);  // empty split: lse = -inf, w = 0
-      W += w;
-      o1 = fmaf(w, rec[s * REC + dim], o1);
-      o2 = fmaf(w, rec[s * REC + D + dim], o2);
-      sf = fmaf(w, rec[s * REC + 2 * D], sf);
+  if (seqlens[b] > 0) {  // a row of length 0 has no records: its output is 0
+    const int2 mt = meta[b * Hkv + kvh];
+    // Every row of nonzero length has its table entry written by this call's
+    // split kernel; an entry outside the records (left by an earlier call
+    // when this one did no work) is not followed.
+    const bool inside = mt.x >= 0 && mt.y >= 1 && static_cast<long long>(mt.x) + mt.y <= nslots;
+    const int nrec = inside ? mt.y : 0;
+    const size_t stride = static_cast<size_t>(G) * REC;
+    const float *rec =
+        recs + static_cast<size_t>(inside ? mt.x : 0) * stride + static_cast<size_t>(gh) * REC;
+    float M = -INFINITY;
+    for (int s = dim; s < nrec; s += D) M = fmaxf(M, rec[s * stride + 2 * D + 1]);
+    M = block_max(M, slot);  // the same value in every thread
+    if (M != -INFINITY) {
+      float W = 0.f, o1 = 0.f, o2 = 0.f, sf = 0.f;
+      for (int base = 0; base < nrec; base += CCH) {
+        const int cnt = min(CCH, nrec - base);
+        const float *rb = rec + static_cast<size_t>(base) * stride;
+        __syncthreads();  // the previous chunk's weights are consumed
+        for (int i = dim; i < cnt; i += D) {
+          const float w = exp2f(rb[i * stride + 2 * D + 1] - M);  // aborted share: lse = -inf, w = 0
+          wsig[0][i] = w;
+          wsig[1][i] = w * rb[i * stride + 2 * D];
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int i = 0; i < cnt; ++i) {
+          const float w = wsig[0][i];
+          W += w;
+          sf += wsig[1][i];
+          o1 = fmaf(w, rb[i * stride + dim], o1);
+          o2 = fmaf(w, rb[i * stride + D + dim], o2);
+        }
+      }
+      const float inv = 1.f / W;
+      o1 *= inv;
+      o2 *= inv;
+      sf *= inv;
+      c = o2 - o1 * sf;  // the correction Sigma rho
+      o = o1 - c;
     }
-    const float inv = 1.f / W;
-    o1 *= inv;
-    o2 *= inv;
-    sf *= inv;
-    c = o2 - o1 * sf;  // the correction Sigma rho
-    o = o1 - c;
   }
   out[static_cast<size_t>(bh) * D + dim] = __float2bfloat16_rn(o);
   if (cor != nullptr) {
@@ -353,7 +564,8 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
 
 cudaError_t launch_decode(const void *q, const void *r, const void *kcache, const void *vcache,
                           const int *seqlens, void *out, float *cor, int B, int Hq, int Hkv,
-                          int nsplit, float *workspace, unsigned *err, cudaStream_t stream) {
+                          int nshare, bool default_share, void *workspace, unsigned *err,
+                          cudaStream_t stream) {
   static thread_local int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -387,19 +599,23 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
   a.q = static_cast<const __nv_bfloat16 *>(q);
   a.r = static_cast<const __nv_bfloat16 *>(r);
   a.seqlens = seqlens;
-  a.ws = workspace;
+  a.meta = static_cast<int2 *>(workspace);
+  a.recs = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_meta_bytes(B, Hkv));
   a.B = B;
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.G = Hq / Hkv;
-  a.nsplit = nsplit;
+  a.nshare = nshare;
+  a.min_keys = default_share ? kDefaultMinKeys : 1;
+  a.align = default_share;
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   a.err = err;
-  decode_split_kernel<<<dim3(Hkv, nsplit, B), THREADS, SMEM_BYTES, stream>>>(mk, mv, a);
+  decode_split_kernel<<<nshare, THREADS, SMEM_BYTES, stream>>>(mk, mv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<B * Hq, D, 0, stream>>>(workspace, static_cast<__nv_bfloat16 *>(out),
-                                                  cor, nsplit);
+  decode_combine_kernel<<<B * Hq, D, 0, stream>>>(a.recs, a.meta, seqlens,
+                                                  static_cast<__nv_bfloat16 *>(out), cor, Hq, Hkv,
+                                                  nshare + B * Hkv);
   return cudaGetLastError();
 }
 

@@ -18,6 +18,9 @@ namespace plx {
 // About two seconds at 2 GHz: far longer than any legitimate wait here.
 constexpr long long kSpinLimitCycles = 1ll << 32;
 constexpr unsigned kErrTimeout = 1u;
+// A kernel found its device-side inputs out of range (decode: the lengths sum
+// to 2^30 tokens or more) and did no work.
+constexpr unsigned kErrBadInput = 2u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

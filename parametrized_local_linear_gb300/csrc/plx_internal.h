@@ -47,10 +47,28 @@ cudaError_t launch_prefill_bwd(const void *q, const void *k, const void *v, cons
                                void *dr, int B, int Hq, int Hkv, int L, void *stats, unsigned *err,
                                cudaStream_t stream);
 
+// Decode over nshare CTAs, each with an equal share of the batch's keys (all
+// sequences and kv heads in one stream). default_share: the default
+// schedule, which also gives every CTA at least 512 keys (fewer CTAs take
+// part in small batches); otherwise min(nshare, keys) CTAs take part.
 // cor ([B, Hq] fp32, |correction| / |o|) may be null.
 cudaError_t launch_decode(const void *q, const void *r, const void *kcache, const void *vcache,
                           const int *seqlens, void *out, float *cor, int B, int Hq, int Hkv,
-                          int nsplit, float *workspace, unsigned *err, cudaStream_t stream);
+                          int nshare, bool default_share, void *workspace, unsigned *err,
+                          cudaStream_t stream);
+
+// Decode workspace: a table of {first record slot, slots} per (sequence, kv
+// head), padded to 256 bytes, then (nshare + B * Hkv) slots of Hq / Hkv
+// records of 2 d + 2 floats. CTA c writes its part of row `row` (sequence,
+// kv head) to slot c + row; a later CTA never holds an earlier row, so the
+// slots of the (CTA, row) pairs that meet are distinct.
+inline size_t decode_meta_bytes(int B, int Hkv) {
+  return (static_cast<size_t>(B) * Hkv * 8 + 255) / 256 * 256;
+}
+inline size_t decode_workspace_bytes(int B, int Hq, int Hkv, int d, int nshare) {
+  const size_t recs = static_cast<size_t>(nshare) * (Hq / Hkv) + static_cast<size_t>(B) * Hq;
+  return decode_meta_bytes(B, Hkv) + recs * (2 * static_cast<size_t>(d) + 2) * sizeof(float);
+}
 
 // Fixed split-record array of the allocation-free decode: 16 MiB of fp32.
 constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;

@@ -70,14 +70,20 @@ def test_decode_rejects_bad_arguments(lib):
     assert f(p, p, p, p, p, p, 2, 32, 2, 128, None) == binding.PLX_ERR_UNSUPPORTED  # G = 16
     assert f(p, p, p, p, p, p, 2, 4, 3, 128, None) == binding.PLX_ERR_INVALID_ARG
     ex = lib.plx_decode_fwd_ex
-    small = lib.plx_decode_workspace_bytes(2, 4, 128, 3) - 4
+    small = lib.plx_decode_workspace_bytes(2, 4, 2, 128, 3) - 4
     assert ex(p, p, p, p, p, p, 2, 4, 2, 128, 3, p, small, None) == binding.PLX_ERR_INVALID_ARG
     assert b"workspace" in lib.plx_last_error_message()
 
 
 def test_workspace_size_formula(lib):
-    assert lib.plx_decode_workspace_bytes(4, 16, 128, 5) == 4 * 16 * 5 * (2 * 128 + 2) * 4
-    assert lib.plx_decode_workspace_bytes(0, 16, 128, 5) == 0
+    # A row table of 8 bytes per (sequence, kv head), padded to 256 bytes, then
+    # (nsplit + B * Hkv) record slots of Hq / Hkv records of 2 d + 2 floats.
+    rec = (2 * 128 + 2) * 4
+    assert lib.plx_decode_workspace_bytes(4, 16, 8, 128, 5) == 256 + (5 + 4 * 8) * 2 * rec
+    assert lib.plx_decode_workspace_bytes(40, 4, 1, 128, 3) == 512 + (3 + 40) * 4 * rec
+    assert lib.plx_decode_workspace_bytes(0, 16, 8, 128, 5) == 0
+    assert lib.plx_decode_workspace_bytes(4, 16, 8, 128, 0) == 0
+    assert lib.plx_decode_workspace_bytes(4, 12, 8, 128, 5) == 0  # Hq not a multiple of Hkv
 
 
 def test_binding_fails_loudly_without_library(monkeypatch):

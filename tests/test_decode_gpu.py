@@ -44,7 +44,7 @@ def test_decode_matches_oracle_all_pairs(lens, Hq, Hkv):
             assert torch.all(out[b] == 0)
 
 
-@pytest.mark.parametrize("nsplit", [1, 3, 7, 64])
+@pytest.mark.parametrize("nsplit", [1, 3, 7, 64, 2000])
 def test_decode_split_count_does_not_change_the_result(nsplit):
     lens = [700, 1, 129, 2048]
     q, r, kc, vc, sl = inputs.decode_inputs(len(lens), 16, 8, 128, lens, torch.bfloat16, 0.05, 77)
@@ -59,7 +59,7 @@ def test_decode_with_caller_workspace():
     lens = [90, 4000]
     q, r, kc, vc, sl = inputs.decode_inputs(2, 4, 2, 128, lens, torch.bfloat16, 0.05, 8)
     nsplit = 5
-    nbytes = plx_decode_workspace_bytes(2, 4, 128, nsplit)
+    nbytes = plx_decode_workspace_bytes(2, 4, 2, 128, nsplit)
     ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=dev)
     out = _decode(q, r, kc, vc, sl, nsplit=nsplit, workspace=ws)
     ref, _ = oracle.decode(q, r, kc, vc, sl)
@@ -95,8 +95,42 @@ def test_decode_full_size_workload_sampled_pairs(w):
 def test_default_split_count_is_sane():
     device()
     n = plx_decode_default_nsplit(64, 8)
-    assert 1 <= n <= 256
-    assert plx_decode_default_nsplit(1, 1) >= n
+    # Two CTAs per SM, whatever the batch.
+    assert n == 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    assert plx_decode_default_nsplit(1, 1) == n
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,nsplit", [
+    ([0, 0, 5, 0, 300, 0], 4, 2, 7),     # empty sequences before, between and after
+    ([1] * 40, 8, 1, 3),                 # one-key sequences: a share holds many rows
+    ([17, 1, 33], 16, 8, 500),           # more shares than keys: one key a share
+    ([2048, 0, 4095], 2, 1, 64),         # shares cut long rows at tile-unaligned keys
+    ([100], 16, 8, 0),                   # default schedule, 800 keys: 2 shares of 400
+    ([3, 700, 9, 1500], 8, 4, 0),        # default schedule across ragged rows
+    ([40] * 64, 16, 8, 0),               # default, one length: 32 shares of 16 whole rows
+    ([0, 100, 100, 0, 100], 4, 2, 0),    # default, one length among empty rows: 3 rows a share
+])
+def test_decode_shares_across_rows(lens, Hq, Hkv, nsplit):
+    """The batch's keys are one stream cut into equal shares; shares start and
+    end inside rows, hold several rows, or hold a single key."""
+    q, r, kc, vc, sl = inputs.decode_inputs(len(lens), Hq, Hkv, 128, lens, torch.bfloat16, 0.05,
+                                            3 * len(lens) + nsplit)
+    out = _decode(q, r, kc, vc, sl, nsplit=nsplit)
+    ref, _ = oracle.decode(q, r, kc, vc, sl)
+    assert_bf16_close(out.double().numpy(), ref, f"decode shares {lens} nsplit {nsplit}")
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.all(out[b] == 0)
+
+
+def test_decode_all_sequences_empty():
+    lens = [0, 0, 0]
+    q, r, kc, vc, sl = inputs.decode_inputs(3, 4, 2, 128, lens, torch.bfloat16, 0.05, 5)
+    kc = torch.zeros(16, 2, 128, dtype=torch.bfloat16)  # a cache holding no sequence's keys
+    vc = torch.zeros_like(kc)
+    for nsplit in (0, 1, 9):
+        out = _decode(q, r, kc, vc, sl, nsplit=nsplit)
+        assert torch.all(out == 0)
 
 
 @pytest.mark.parametrize("lens,Hq,Hkv", [
