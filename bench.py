@@ -385,6 +385,13 @@ def main():
     # stream while the previous sequence's prefill runs (one plx_prefill_fwd
     # call per sequence), the decode's new q, r follow, and each output comes
     # back while later work runs. A step ends when its last copy has landed.
+    # Measured on GB300: the host link moves about 210 GB/s host to device and
+    # 192 GB/s back, the same with 1 to 8 DMA streams or an SM copy kernel, so
+    # the copies, not the kernels, bound this leg (201 MB up, 67 MB back: 1.31
+    # ms of link time against 1.45 ms a step). Sending the outputs back on a
+    # second stream, concurrently with the inputs, was slower (1.51 ms): both
+    # directions at once drop to about 169 GB/s each, and the inputs are on
+    # the critical path.
     hq = [t.cpu().pin_memory() for t in (q, k, v, r)]
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hd = [t.cpu().pin_memory() for t in (dq, dr)]
@@ -621,7 +628,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "method": "one prefill call per sequence; host copies on a second stream, "
-                          "overlapped with the kernels, inside the timing"},
+                          "overlapped with the kernels, inside the timing; the host link "
+                          "(about 210 GB/s up, 192 GB/s down) bounds it"},
         "gpu_launches": 3 * K,
         "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev),
