@@ -477,11 +477,16 @@ def main():
 
         def launch_cold_s(fn, n):
             """Mean seconds per call of fn() with L2 flushed before each call
-            (a 512 MB write outside the timed interval), 3 untimed calls first."""
+            (a 512 MB write outside the timed interval), 3 untimed calls first.
+            Eight flushes go ahead of the loop so that the host, enqueueing
+            through the Python binding, stays ahead of the GPU: a gap between
+            the first event and a short kernel would otherwise be timed."""
             for _ in range(3):
                 fn()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(n)]
+            for _ in range(8):
+                l2_flush.zero_()
             for e0, e1 in evs:
                 l2_flush.zero_()
                 e0.record(stream)
