@@ -242,6 +242,11 @@ __global__ void __launch_bounds__(THREADS)
     fence_mbar_init();
   }
   __syncthreads();
+  // The combine kernel is launched as a programmatic dependent of this grid:
+  // its blocks may be scheduled once every CTA here has passed this point,
+  // and they wait (griddepcontrol.wait) for this grid to complete before
+  // reading a record, so their launch overlaps this grid's tail.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Plan pl = *plan;
   if (pl.b0 < 0) return;  // no share: more CTAs than the batch needs
   const Abort ab{abort_flag, a.err};
@@ -487,6 +492,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float *__restri
                                                           int Hkv, int nslots) {
   __shared__ float wsig[2][CCH];
   __shared__ float slot[D / 32];
+  // Launched as a programmatic dependent of the split kernel: wait for that
+  // grid to complete (its records and row table visible) before any read.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x, dim = threadIdx.x;
   const int b = bh / Hq, h = bh - b * Hq, G = Hq / Hkv;
   const int kvh = h / G, gh = h - kvh * G;
@@ -613,9 +621,19 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
   decode_split_kernel<<<nshare, THREADS, SMEM_BYTES, stream>>>(mk, mv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<B * Hq, D, 0, stream>>>(a.recs, a.meta, seqlens,
-                                                  static_cast<__nv_bfloat16 *>(out), cor, Hq, Hkv,
-                                                  nshare + B * Hkv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B * Hq);
+  cfg.blockDim = dim3(D);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float *>(a.recs),
+                         static_cast<const int2 *>(a.meta), seqlens,
+                         static_cast<__nv_bfloat16 *>(out), cor, Hq, Hkv, nshare + B * Hkv);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
