@@ -1,5 +1,5 @@
-// Parallax decode: split-KV streaming over a packed bf16 KV cache, then a
-// log-sum-exp combine of the per-split partial results.
+// Parallax decode: equal shares of the batch's key stream streamed from a
+// packed bf16 KV cache, then a log-sum-exp combine of the partial results.
 //
 // The method ("Parallax: parametrized local linear attention for language
 // modeling", sections "Core mechanism" and "Hardware-aware algorithm") adds a
@@ -8,13 +8,15 @@
 // instructions so the cache is read from HBM once for both branches. This
 // kernel does the same on sm_103a with warp-level mma.sync:
 //
-//   CTA (split s, kv head g, sequence b), 4 consumer warps + 1 producer warp.
+//   One wave of CTAs (two per SM), each with an equal share of the keys of
+//   all (sequence, kv head) rows taken as one stream; a share is cut at row
+//   boundaries into items. 4 consumer warps + 1 producer warp per CTA.
 //   Producer: one thread issues tiled TMA loads of 16-token x 64-dim boxes of
 //     the K and V cache (3-D tensor maps over [tokens, Hkv, d]) into a ring of
 //     8 shared-memory stages, 128-byte swizzled so ldmatrix is bank-conflict
 //     free; completion is counted in bytes on per-stage mbarriers. Four 2 KB
 //     requests move an 8 KB stage (per-row 256-byte copies were limited by
-//     the TMA request rate).
+//     the TMA request rate). The ring runs on across items.
 //   Consumers: stages are dealt round-robin to the 4 warps, two per warp. For each 16 keys
 //     one m16n8k16 product gives all four dot-product families at once: A rows
 //     0..G-1 hold the G query heads' q, rows 8..8+G-1 their probes r, so the
@@ -23,13 +25,14 @@
 //     value product (rows g: P -> O1, rows g + 8: P*T -> O2), again in
 //     registers, with V^T read by ldmatrix.trans.
 //   Each warp runs the online-softmax recurrence (running max m, denominator
-//   l, sigma = sum p t, O1 and O2 accumulators, all rescaled together); the
-//   warps are merged in shared memory and the CTA writes one partial record
-//   per query head: (O1/l, O2/l, sigma/l, log2-sum-exp) in fp32.
+//   l, sigma = sum p t, O1 and O2 accumulators, all rescaled together); at
+//   the end of an item the warps are merged in shared memory and the CTA
+//   writes one partial record per query head: (O1/l, O2/l, sigma/l,
+//   log2-sum-exp) in fp32.
 //
 // The combine kernel merges the records of a (sequence, head) with weights
 // 2^(lse_s - max) and only then forms o = O1 - O2 + O1 * s. Combining final
-// per-split outputs would be wrong: O1 * s is bilinear in the partial sums.
+// per-share outputs would be wrong: O1 * s is bilinear in the partial sums.
 #include <math.h>
 
 #include <mutex>

@@ -79,7 +79,7 @@ class DecodeShape:
 
     def bytes_moved(self, seqlens=None) -> int:
         """Algorithmic HBM bytes: K and V cache read once, q and r read, out
-        written (the split workspace is overhead and not counted)."""
+        written (the decode workspace is overhead and not counted)."""
         lens = self.seqlens() if seqlens is None else seqlens
         esz = torch.finfo(self.dtype).bits // 8
         kv = 2 * int(lens.sum()) * self.Hkv * self.d * esz

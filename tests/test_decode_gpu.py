@@ -1,4 +1,5 @@
-"""GPU decode (split-KV + log-sum-exp combine) parity against the fp64 oracle."""
+"""GPU decode (equal shares of the batch's key stream + log-sum-exp combine)
+parity against the fp64 oracle."""
 import random
 
 import numpy as np
@@ -45,7 +46,7 @@ def test_decode_matches_oracle_all_pairs(lens, Hq, Hkv):
 
 
 @pytest.mark.parametrize("nsplit", [1, 3, 7, 64, 2000])
-def test_decode_split_count_does_not_change_the_result(nsplit):
+def test_decode_share_count_does_not_change_the_result(nsplit):
     lens = [700, 1, 129, 2048]
     q, r, kc, vc, sl = inputs.decode_inputs(len(lens), 16, 8, 128, lens, torch.bfloat16, 0.05, 77)
     base = _decode(q, r, kc, vc, sl, nsplit=1).float()
@@ -92,7 +93,7 @@ def test_decode_full_size_workload_sampled_pairs(w):
     assert torch.isfinite(out).all()
 
 
-def test_default_split_count_is_sane():
+def test_default_share_count_is_sane():
     device()
     n = plx_decode_default_nsplit(64, 8)
     # Two CTAs per SM, whatever the batch.

@@ -1,7 +1,7 @@
 """The allocation-free decode entry point (plx_decode_fwd_noalloc).
 
 Some callers cannot allocate device memory while they call into this
-library; this entry point serves them by keeping its split records in a fixed
+library; this entry point serves them by keeping its partial records in a fixed
 device array. It must give the same result as plx_decode_fwd, call after
 call, because the array is reused and keeps the previous call's contents.
 This file is named so that pytest collects it last."""
@@ -48,7 +48,7 @@ def test_noalloc_decode_rejects_too_many_records():
     device()
     z = torch.zeros(16, device="cuda", dtype=torch.bfloat16)
     p = ctypes.c_void_p(z.data_ptr())
-    # B * Hq * (2 * 128 + 2) * 4 bytes > 16 MiB even with one split
+    # the row table plus B * Hq records of (2 * 128 + 2) * 4 bytes > 16 MiB even with one share
     st = binding.lib().plx_decode_fwd_noalloc(p, p, p, p, p, p, 8192, 8, 8, 128, None)
     assert st == binding.PLX_ERR_UNSUPPORTED
     assert b"fixed array" in binding.lib().plx_last_error_message()
