@@ -6,37 +6,45 @@
 // epilogue that writes every output element straight into the per-head
 // layouts the attention kernels read ([B, H, L, 128]).
 //
-// Persistent GEMM, one CTA per SM, in clusters of two. A tile is 128 token
-// rows x 256 output features (two heads); the two CTAs of a cluster take
-// neighbouring token tiles of the same feature tile, and each loads its own
-// x tile and half of the shared W tile, multicast to both: a stage then
-// costs each SM 32 KB of L2 reads instead of 48 KB for 512 tensor cycles
-// (the single-CTA form was bound by L2-to-SM bandwidth, tensor pipe 58%
-// busy). A stage is refilled only when the UMMAs of both CTAs are done with
-// it: each CTA's UMMA thread commits the stage's release to the empty
-// barrier of both (count 2). The K loop walks the model dimension in
-// 64-element stages (one 128-byte swizzle atom) through a 4-stage TMA ring.
-// The two 256-column fp32 accumulators in TMEM alternate between tiles, so
-// the epilogue of one tile overlaps the UMMAs of the next. 6 warps:
-//   warp 0      TMA producer (x tile 128 x 64; W rows 128 x 64, multicast)
-//   warp 1      TMEM allocator; one thread issues the 128 x 256 x 16 UMMAs
-//   warps 2..5  epilogue: thread = token row = TMEM lane; 32-column chunks
-//               are converted to bf16 (round to nearest even) and stored as
-//               64 contiguous bytes of one head row.
+// Persistent GEMM, one CTA per SM, in clusters of two that work as a CTA
+// pair on the two-SM tensor-core form (tcgen05 .cta_group::2). A tile is 256
+// token rows x 256 output features (two heads): each CTA of the pair loads
+// its own 128 token rows of x and its half (128 rows) of the W tile, and the
+// leader CTA issues 256 x 256 x 16 UMMAs that read A from both CTAs and B
+// half from each, with the accumulator rows of each CTA in its own TMEM.
+// Per SM a stage is then 32 KB of TMA writes and 32 KB of UMMA operand reads
+// for 512 tensor cycles, 128 bytes per cycle: the single-SM form needed 192
+// (a 48 KB stage written and read again) and ran the tensor pipe at most
+// two-thirds busy, bound by shared-memory bandwidth. The K loop walks the
+// model dimension in 64-element stages (one 128-byte swizzle atom) through a
+// 6-stage TMA ring whose completion both CTAs count on the leader's
+// barriers; the leader's UMMA commits release a stage in both CTAs. The two
+// 256-column fp32 accumulators in TMEM alternate between tiles, so the
+// epilogue of one tile overlaps the UMMAs of the next. 10 warps:
+//   warp 0      TMA producer (x tile 128 x 64; this CTA's 128 W rows x 64)
+//   warp 1      TMEM allocator (with the peer); in the leader one thread
+//               issues the pair UMMAs
+//   warps 2..9  epilogue, two warps per TMEM lane quarter, each with half
+//               of the 256 columns: thread = token row = TMEM lane;
+//               32-column chunks are converted to bf16 (round to nearest
+//               even) and stored as 64 contiguous bytes of one head row.
+//               With one warp per quarter the stores of a tile outlasted the
+//               next tile's UMMAs at model dim 1024.
 #include "plx_device.cuh"
 #include "plx_internal.h"
 
 namespace plx {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, NST = 4, HD = 128;
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_BYTES = BN * BK * 2;        // 32 KB
-constexpr int STAGE = A_BYTES + B_BYTES;    // 48 KB
+constexpr int BM = 128, BN = 256, BK = 64, NST = 6, HD = 128;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB: this CTA's 128 token rows
+constexpr int B_BYTES = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of the 256 W rows
+constexpr int STAGE = A_BYTES + B_BYTES;    // 32 KB
 constexpr int OFF_BAR = NST * STAGE;        // 196608
 constexpr int NBAR = 2 * NST + 4 + 1;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
-constexpr int THREADS = 32 * 6;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 32 * (2 + EPI_WARPS);
 
 struct ProjArgs {
   __nv_bfloat16 *q, *k, *v, *r;
@@ -52,10 +60,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-  uint64_t *full = bars;                // [NST] stage loaded
-  uint64_t *empty = full + NST;         // [NST] count 2: both CTAs' UMMAs done with the stage
+  uint64_t *full = bars;                // [NST] leader: both CTAs' parts of the stage loaded
+  uint64_t *empty = full + NST;         // [NST] the pair UMMAs are done with the stage
   uint64_t *acc_full = empty + NST;     // [2] accumulator complete
-  uint64_t *acc_empty = acc_full + 2;   // [2] count 128: accumulator read by the epilogue
+  uint64_t *acc_empty = acc_full + 2;   // [2] leader: both CTAs' epilogue threads read it
   uint64_t *drain = acc_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -64,11 +72,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 2);
+      mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&acc_full[x]), 1);
-      mbar_init(smem_u32(&acc_empty[x]), 128);
+      mbar_init(smem_u32(&acc_empty[x]), 2 * 32 * EPI_WARPS);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -79,16 +87,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_tensormap(&tm_w);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  // Both CTAs' barriers must be initialised before either multicasts.
+  // Both CTAs' barriers must be initialised before either signals the other.
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const Abort ab{abort_flag, a.err};
   const int crank = static_cast<int>(cluster_ctarank());
+  const bool leader = crank == 0;
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
   if (warp == 0) {
@@ -101,31 +110,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kk = 0; kk < a.kt; ++kk, ++g) {
           const int st = g % NST;
           if (g >= NST && !mbar_wait(smem_u32(&empty[st]), ((g / NST) - 1) & 1, ab)) { ok = false; break; }
-          const uint32_t fb = smem_u32(&full[st]);
+          // The leader's barrier counts both CTAs' 32 KB.
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full[st]), 2 * STAGE);
+          const uint32_t fb = mapa_shared(smem_u32(&full[st]), 0);
           const uint32_t base = smem_u32(smem + st * STAGE);
-          // Own x tile (16 KB) + both W halves (one from each CTA): 48 KB.
-          mbar_arrive_expect_tx(fb, STAGE);
-          tma_load_3d(base, &tm_x, kk * BK, m0, 0, fb);
-          tma_load_3d_mc(base + A_BYTES + crank * (B_BYTES / 2), &tm_w, kk * BK, n0 + crank * (BN / 2), 0,
-                         fb, 0x3);
+          tma_load_3d_pair(base, &tm_x, kk * BK, m0, 0, fb);
+          tma_load_3d_pair(base + A_BYTES, &tm_w, kk * BK, n0 + crank * (BN / 2), 0, fb);
           issued = g + 1;
         }
       }
-      if (ab.raised())
+      // Only the leader can wait on the stage barriers; they count the
+      // peer's copies too, and the peer waits for the leader at the end.
+      if (ab.raised() && leader)
         for (int x = max(0, issued - NST); x < issued; ++x)
           mbar_wait_drain(smem_u32(&full[x % NST]), (x / NST) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------------------ UMMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0);
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, 0);
       const uint64_t adesc0 = smem_desc_sw128(smem_u32(smem), 16, 1024);
       const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + A_BYTES), 16, 1024);
       int g = 0, it = 0;
       bool ok = true;
       for (int tp = cid; ok && tp < a.npairs; tp += ncl, ++it) {
         const int buf = it & 1;
-        // The accumulator's previous tile must have been read out.
+        // The accumulator's previous tile must have been read out by both CTAs.
         if (it >= 2 && !mbar_wait(smem_u32(&acc_empty[buf]), ((it >> 1) - 1) & 1, ab)) break;
         tc_fence_after();
         const uint32_t d = tbase + buf * BN;
@@ -135,17 +145,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint64_t ad = adesc0 + st * (STAGE >> 4), bd = bdesc0 + st * (STAGE >> 4);
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks) umma_ss(d, ad + ks * 2, bd + ks * 2, idesc, (kk > 0 || ks > 0));
-          umma_commit_mc(smem_u32(&empty[st]), 0x3);  // release the stage in both CTAs
+          for (int ks = 0; ks < BK / 16; ++ks)
+            umma_ss_pair(d, ad + ks * 2, bd + ks * 2, idesc, (kk > 0 || ks > 0));
+          umma_commit_pair_mc(smem_u32(&empty[st]), 0x3);  // release the stage in both CTAs
         }
-        if (ok) umma_commit(smem_u32(&acc_full[buf]));
+        if (ok) umma_commit_pair_mc(smem_u32(&acc_full[buf]), 0x3);
       }
-      umma_commit(smem_u32(drain));
+      umma_commit_pair_mc(smem_u32(drain), 0x1);
       mbar_wait_drain(smem_u32(drain), 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int qw = warp & 3, row = qw * 32 + lane;
+    const int c0 = ((warp - 2) >> 2) * (BN / 64);  // first of this warp's 32-column chunks
     const uint32_t tl = tbase + (static_cast<uint32_t>(qw * 32) << 16);
     const int fq = a.Hq * HD, fk = fq + a.Hkv * HD, fv = fk + a.Hkv * HD;
     int it = 0;
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool valid = t < a.T;
       const int b = valid ? t / a.L : 0, l = valid ? t - b * a.L : 0;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = c0; c < c0 + BN / 64; ++c) {
         float vals[32];
         tmem_ld32(tl + buf * BN + c * 32, vals);
         tmem_wait_ld();
@@ -183,18 +195,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&acc_empty[buf]));
+      mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[buf]), 0));
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // Every pair UMMA has completed (the leader drained them; the peer's
+  // epilogue saw the last accumulator) once both CTAs are here.
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tbase, 512);
+    tmem_dealloc_pair(tbase, 512);
   }
-  // Neither CTA leaves while the other may still multicast into it or
-  // arrive on its barriers.
+  // Neither CTA leaves while the other may still signal its barriers.
   cluster_sync_all();
 }
 
