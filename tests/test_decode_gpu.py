@@ -155,3 +155,25 @@ def test_decode_cor_matches_oracle(lens, Hq, Hkv):
     for b, n in enumerate(lens):
         if n == 0:
             assert torch.all(cor[b] == 0)  # no keys: o = 0 and the ratio is defined as 0
+
+
+def test_decode_lengths_past_the_token_extent_are_reported():
+    """Lengths are on the device, so the host cannot check their sum; a batch
+    whose lengths sum to 2^30 tokens or more (past the cache maps' extent) does
+    no work and is reported by plx_check_device_error, and the next call runs
+    normally. The cache is never read in that call, so a small one stands in."""
+    from parametrized_local_linear_gb300 import PlxError, binding
+    dev = device()
+    q, r, kc, vc, _ = inputs.decode_inputs(2, 4, 2, 128, [16, 16], torch.bfloat16, 0.05, 3)
+    qd, rd, kd, vd = _to(dev, q, r, kc, vc)
+    big = torch.tensor([1 << 29, 1 << 29], dtype=torch.int32, device=dev)
+    out = torch.empty_like(qd)
+    plx_decode_fwd(qd, rd, kd, vd, big, out)
+    with pytest.raises(PlxError) as exc:
+        plx_check_device_error()
+    assert exc.value.status == binding.PLX_ERR_INVALID_ARG
+    # The error word was cleared; an ordinary call on the same device works.
+    sl = torch.tensor([16, 16], dtype=torch.int32)
+    got = _decode(q, r, kc, vc, sl)
+    ref, _ = oracle.decode(q, r, kc, vc, sl)
+    assert_bf16_close(got.double().numpy(), ref, "decode after a reported error")
