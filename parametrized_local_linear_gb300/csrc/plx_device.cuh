@@ -405,10 +405,14 @@ __device__ __forceinline__ uint64_t f2(float lo, float hi) {
   return r;
 }
 __device__ __forceinline__ float f2lo(uint64_t v) {
-  return __uint_as_float(static_cast<uint32_t>(v));
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
 }
 __device__ __forceinline__ float f2hi(uint64_t v) {
-  return __uint_as_float(static_cast<uint32_t>(v >> 32));
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
 }
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t r;
