@@ -235,6 +235,9 @@ plx_status plx_decode_fwd_cor(const void *q, const void *r, const void *kcache, 
  *     16 MiB, else PLX_ERR_UNSUPPORTED and nothing runs.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     The address is kept per device together with the id of the CUDA
+ *     context it belongs to; after a cudaDeviceReset the next call runs in a
+ *     new context and looks the address up again (outside a capture too).
  *   - Every call shares the array: calls that overlap on the GPU race and must
  *     be serialised by the caller. The array needs no clearing between calls
  *     (each call writes every record it reads).

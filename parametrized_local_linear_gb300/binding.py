@@ -283,6 +283,42 @@ def plx_prefill_fwd_f32(q, k, v, r, out=None, lse=None, stream=None):
     return _prefill(lib().plx_prefill_fwd_f32, torch.float32, q, k, v, r, out, lse, stream)
 
 
+def _decode_shapes(q, r, kcache, vcache, seqlens, out=None, cor=None):
+    """Shape checks shared by every decode call, made before any device check
+    or launch: a short ``seqlens``, ``out`` or ``cor`` would otherwise let the
+    kernels read or write past the end of a buffer."""
+    if q.dim() != 3:
+        raise ValueError(f"q must be [B, Hq, d], got shape {tuple(q.shape)}")
+    B, Hq, d = q.shape
+    if tuple(r.shape) != tuple(q.shape):
+        raise ValueError(f"r has shape {tuple(r.shape)}, expected the shape of q {tuple(q.shape)}")
+    if kcache.dim() != 3 or kcache.shape[2] != d:
+        raise ValueError(f"kcache must be [T, Hkv, {d}], got shape {tuple(kcache.shape)}")
+    if tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError(f"vcache has shape {tuple(vcache.shape)}, expected the shape of kcache "
+                         f"{tuple(kcache.shape)}")
+    if seqlens.dim() != 1 or seqlens.shape[0] != B:
+        raise ValueError(f"seqlens must have shape ({B},), got {tuple(seqlens.shape)}")
+    if out is not None and tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"out has shape {tuple(out.shape)}, expected the shape of q {tuple(q.shape)}")
+    if cor is not None and tuple(cor.shape) != (B, Hq):
+        raise ValueError(f"cor has shape {tuple(cor.shape)}, expected ({B}, {Hq})")
+
+
+def _decode_tensors(q, r, kcache, vcache, seqlens, out, cor=None):
+    _decode_shapes(q, r, kcache, vcache, seqlens, out, cor)
+    _need(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    for name, t in (("r", r), ("kcache", kcache), ("vcache", vcache)):
+        _need(t, name, torch.bfloat16, 3, dev)
+    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    if out is not None:
+        _need(out, "out", torch.bfloat16, 3, dev)
+    if cor is not None:
+        _need(cor, "cor", torch.float32, 2, dev)
+    return dev
+
+
 def plx_decode_fwd(q, r, kcache, vcache, seqlens, out=None, nsplit=0, workspace=None,
                    stream=None):
     """Parallax decode over a packed ragged KV cache (see include/plx.h).
@@ -291,21 +327,11 @@ def plx_decode_fwd(q, r, kcache, vcache, seqlens, out=None, nsplit=0, workspace=
     seqlens: int32 [B] on the device. ``nsplit``/``workspace`` select
     plx_decode_fwd_ex; the defaults call plx_decode_fwd. Returns out.
     """
-    _need(q, "q", torch.bfloat16, 3)
-    dev = q.device
-    _need(r, "r", torch.bfloat16, 3, dev)
-    _need(kcache, "kcache", torch.bfloat16, 3, dev)
-    _need(vcache, "vcache", torch.bfloat16, 3, dev)
-    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    dev = _decode_tensors(q, r, kcache, vcache, seqlens, out)
     B, Hq, d = q.shape
     Hkv = kcache.shape[1]
-    if tuple(r.shape) != tuple(q.shape) or tuple(vcache.shape) != tuple(kcache.shape):
-        raise ValueError("r must match q and vcache must match kcache")
-    if kcache.shape[2] != d or seqlens.shape[0] != B:
-        raise ValueError("kcache must be [T, Hkv, d] and seqlens [B]")
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, 3, dev)
     L = lib()
     with torch.cuda.device(dev):
         s = _stream(stream, dev)
@@ -329,11 +355,9 @@ def plx_decode_fwd_noalloc(q, r, kcache, vcache, seqlens, out, stream=None):
     """Decode through the entry point that allocates nothing (see include/plx.h):
     the partial records go to the library's fixed device array. ``out`` must be
     given (bf16 [B, Hq, d]); returns it."""
-    _need(q, "q", torch.bfloat16, 3)
-    dev = q.device
-    for name, t in (("r", r), ("kcache", kcache), ("vcache", vcache), ("out", out)):
-        _need(t, name, torch.bfloat16, 3, dev)
-    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    if out is None:
+        raise ValueError("out must be given: this entry point allocates nothing")
+    dev = _decode_tensors(q, r, kcache, vcache, seqlens, out)
     B, Hq, d = q.shape
     with torch.cuda.device(dev):
         st = lib().plx_decode_fwd_noalloc(q.data_ptr(), r.data_ptr(), kcache.data_ptr(),
@@ -347,24 +371,12 @@ def plx_decode_fwd_cor(q, r, kcache, vcache, seqlens, out=None, cor=None, stream
     """Decode that also writes the correction-to-output ratio |Sigma rho| / |o|
     per (sequence, head) (see include/plx.h). ``cor`` is fp32 [B, Hq]
     (allocated if None). Returns (out, cor)."""
-    _need(q, "q", torch.bfloat16, 3)
-    dev = q.device
-    for name, t in (("r", r), ("kcache", kcache), ("vcache", vcache)):
-        _need(t, name, torch.bfloat16, 3, dev)
-    _need(seqlens, "seqlens", torch.int32, 1, dev)
+    dev = _decode_tensors(q, r, kcache, vcache, seqlens, out, cor)
     B, Hq, d = q.shape
-    if tuple(r.shape) != tuple(q.shape) or tuple(vcache.shape) != tuple(kcache.shape):
-        raise ValueError("r must match q and vcache must match kcache")
-    if kcache.shape[2] != d or seqlens.shape[0] != B:
-        raise ValueError("kcache must be [T, Hkv, d] and seqlens [B]")
     if out is None:
         out = torch.empty_like(q)
     if cor is None:
         cor = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-    _need(out, "out", torch.bfloat16, 3, dev)
-    _need(cor, "cor", torch.float32, 2, dev)
-    if tuple(out.shape) != tuple(q.shape) or tuple(cor.shape) != (B, Hq):
-        raise ValueError("out must have the shape of q and cor be [B, Hq]")
     with torch.cuda.device(dev):
         st = lib().plx_decode_fwd_cor(q.data_ptr(), r.data_ptr(), kcache.data_ptr(),
                                       vcache.data_ptr(), seqlens.data_ptr(), out.data_ptr(),

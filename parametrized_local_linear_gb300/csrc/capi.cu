@@ -38,8 +38,15 @@ __device__ unsigned g_plx_device_error = 0;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// Address of the error word per device, with the id of the context it was
+// resolved in: a device reset destroys that context, and the next call
+// resolves the address again in the new one.
 unsigned *g_err_ptr[kMaxDevices] = {};
+unsigned long long g_err_ctx[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
 
 int current_device() {
   int dev = 0;
@@ -68,14 +75,41 @@ __global__ void timeout_probe_kernel(long long limit, unsigned *err) {
 
 namespace plx {
 
+unsigned long long context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 unsigned *device_error_word() {
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long ctx = context_id();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_err_ptr[dev] == nullptr) {
+  if (g_err_ptr[dev] == nullptr || ctx == 0 || g_err_ctx[dev] != ctx) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_plx_device_error) != cudaSuccess) return nullptr;
     g_err_ptr[dev] = static_cast<unsigned *>(p);
+    g_err_ctx[dev] = ctx;
   }
   return g_err_ptr[dev];
 }

@@ -577,14 +577,13 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
                           const int *seqlens, void *out, float *cor, int B, int Hq, int Hkv,
                           int nshare, bool default_share, void *workspace, unsigned *err,
                           cudaStream_t stream) {
-  static thread_local int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
+  static thread_local unsigned long long configured_ctx = 0;
+  const unsigned long long ctx = context_id();
+  if (ctx == 0 || configured_ctx != ctx) {
     cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_ctx = ctx;
   }
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorInvalidValue;
@@ -658,7 +657,11 @@ static __device__ __align__(256) float g_decode_noalloc_scratch[kNoAllocScratchF
 
 namespace {
 std::mutex g_noalloc_mu;
+// The array's address per device and the id of the context it was looked up
+// in; a device reset destroys that context (and the array with it), and the
+// next call looks the address up again in the new context.
 float *g_noalloc_ptr[64] = {};
+unsigned long long g_noalloc_ctx[64] = {};
 }  // namespace
 
 cudaError_t noalloc_scratch(float **ptr) {
@@ -666,12 +669,14 @@ cudaError_t noalloc_scratch(float **ptr) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = context_id();
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (g_noalloc_ptr[dev] == nullptr || ctx == 0 || g_noalloc_ctx[dev] != ctx) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_noalloc_ptr[dev] = static_cast<float *>(p);
+    g_noalloc_ctx[dev] = ctx;
   }
   *ptr = g_noalloc_ptr[dev];
   return cudaSuccess;

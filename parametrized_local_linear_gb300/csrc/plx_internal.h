@@ -21,6 +21,12 @@ EncodeTiledFn encode_tiled_fn();
 
 int sm_count();
 
+// Unique id of the current CUDA context (0 if none is current or the driver
+// cannot say). Set-up that belongs to a context (kernel attributes, device
+// addresses of the library's own arrays) is cached under this id and redone
+// when it changes, e.g. after cudaDeviceReset destroyed the old context.
+unsigned long long context_id();
+
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *r,
                                float *out, float *lse, int B, int Hq, int Hkv, int L, int d,
                                unsigned *err, cudaStream_t stream);

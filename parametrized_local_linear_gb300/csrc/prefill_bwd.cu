@@ -692,17 +692,16 @@ cudaError_t launch_prefill_bwd(const void *q, const void *k, const void *v, cons
                                const float *sbar, const void *dout, void *dq, void *dk, void *dv,
                                void *dr, int B, int Hq, int Hkv, int L, void *stats, unsigned *err,
                                cudaStream_t stream) {
-  static thread_local int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
+  static thread_local unsigned long long configured_ctx = 0;
+  const unsigned long long ctx = context_id();
+  if (ctx == 0 || configured_ctx != ctx) {
     cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          qk::SMEM_BYTES);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kv::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_ctx = ctx;
   }
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorInvalidValue;

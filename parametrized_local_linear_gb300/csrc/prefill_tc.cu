@@ -514,14 +514,13 @@ bool make_head_rows_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, in
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const void *r, void *out,
                               float *lse, float *cor, void *o1, float *sbar, int B, int Hq, int Hkv,
                               int L, int Lk, unsigned *err, cudaStream_t stream) {
-  static thread_local int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
+  static thread_local unsigned long long configured_ctx = 0;
+  const unsigned long long ctx = context_id();
+  if (ctx == 0 || configured_ctx != ctx) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_ctx = ctx;
   }
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorInvalidValue;

@@ -231,14 +231,13 @@ bool make_rows_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, long lo
 cudaError_t launch_qkvr_proj(const void *x, const void *w, void *q, void *k, void *v, void *r,
                              int B, int L, int D, int Hq, int Hkv, unsigned *err,
                              cudaStream_t stream) {
-  static thread_local int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
+  static thread_local unsigned long long configured_ctx = 0;
+  const unsigned long long ctx = context_id();
+  if (ctx == 0 || configured_ctx != ctx) {
     cudaError_t e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    configured_device = dev;
+    configured_ctx = ctx;
   }
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorInvalidValue;
