@@ -19,6 +19,7 @@ import scipy.special
 import torch
 
 import oracle
+from oracle import expanded
 from parametrized_local_linear_gb300 import inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -128,32 +129,46 @@ def test_uniform_weights_give_population_covariance():
     np.testing.assert_allclose(sig, ref, rtol=0, atol=1e-13)
 
 
-def _dense_streaming_identity(q, k, v, r):
-    """o = O1 - O2 + O1*s from dense matrices: P = exp(S - rowmax) on the
-    causal window, O1 = P V / l, O2 = (P*T) V / l, s = rowsum(P*T) / l,
-    T = R K^T (unscaled)."""
-    B, Hq, L, d = q.shape
-    G = Hq // k.shape[1]
-    q = q.numpy(); r = r.numpy()
-    k = np.repeat(k.numpy(), G, axis=1); v = np.repeat(v.numpy(), G, axis=1)
-    S = q @ k.transpose(0, 1, 3, 2) / math.sqrt(d)
-    causal = np.tril(np.ones((L, L), dtype=bool))
-    S = np.where(causal, S, -np.inf)
-    P = np.exp(S - S.max(-1, keepdims=True))
-    ell = P.sum(-1, keepdims=True)
-    T = r @ k.transpose(0, 1, 3, 2)
-    PT = P * T
-    O1 = P @ v / ell
-    O2 = PT @ v / ell
-    s = PT.sum(-1, keepdims=True) / ell
-    return O1 - O2 + O1 * s
+@pytest.mark.parametrize("d,L,Lk,Hq,Hkv,block", [
+    (4, 16, 16, 2, 2, 16), (8, 33, 33, 4, 2, 7), (64, 64, 64, 4, 1, 64), (8, 20, 45, 4, 2, 6)])
+def test_expanded_form_matches_the_explicit_oracle(d, L, Lk, Hq, Hkv, block):
+    """The expanded fp64 form O1 - O2 + O1*s (dense matrices, query rows in
+    blocks) against the explicit-Sigma oracle: every row, lse too, with a
+    chunk offset in the last case. A dropped term, a wrong sign, an unscaled
+    score or a wrong causal window in either would show here."""
+    q, k, v, r = _small(B=2, Hq=Hq, Hkv=Hkv, L=Lk, d=d, seed=d + L)
+    q, r = q[:, :, Lk - L:], r[:, :, Lk - L:]
+    out, lse, cor = oracle.prefill(q, k, v, r, with_cor=True)
+    eo, e_lse, _, _, ecor = expanded.prefill(q, k, v, r, row_block=block, with_parts=True)
+    np.testing.assert_allclose(eo, out, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(e_lse, lse, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ecor, cor, rtol=1e-10, atol=1e-12)
 
 
-@pytest.mark.parametrize("d,L,Hq,Hkv", [(4, 16, 2, 2), (8, 33, 4, 2), (64, 64, 4, 1)])
-def test_matches_dense_streaming_identity(d, L, Hq, Hkv):
-    q, k, v, r = _small(B=2, Hq=Hq, Hkv=Hkv, L=L, d=d, seed=d + L)
-    out, _ = oracle.prefill(q, k, v, r)
-    np.testing.assert_allclose(out, _dense_streaming_identity(q, k, v, r), rtol=0, atol=1e-11)
+def test_expanded_parts_against_library_routines():
+    """o^SA of the expanded form is torch's causal SDPA (fp64, GQA by repeat);
+    sbar is rho . mu with mu the softmax-weighted key mean from numpy."""
+    q, k, v, r = _small(B=1, Hq=4, Hkv=2, L=19, d=8, seed=71)
+    _, _, osa, sbar, _ = expanded.prefill(q, k, v, r, row_block=5, with_parts=True)
+    kk, vv = k.repeat_interleave(2, dim=1), v.repeat_interleave(2, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=True)
+    np.testing.assert_allclose(osa, ref.numpy(), rtol=0, atol=1e-12)
+    for h, i in ((0, 0), (1, 7), (3, 18)):
+        w = scipy.special.softmax(kk[0, h, :i + 1].numpy() @ q[0, h, i].numpy() / math.sqrt(8))
+        mu = np.average(kk[0, h, :i + 1].numpy(), axis=0, weights=w)
+        assert abs(sbar[0, h, i] - r[0, h, i].numpy() @ mu) < 1e-12
+
+
+def test_expanded_decode_matches_the_explicit_oracle():
+    lens = [5, 0, 17, 1, 40]
+    q, r, kc, vc, sl = inputs.decode_inputs(len(lens), 4, 2, 8, lens, torch.float64, 0.3, 9)
+    out, lse, cor = oracle.decode(q, r, kc, vc, sl, with_cor=True)
+    eo, e_lse, ecor = expanded.decode(q, r, kc, vc, sl, with_cor=True)
+    np.testing.assert_allclose(eo, out, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(ecor, cor, rtol=1e-10, atol=1e-12)
+    live = np.array(lens) > 0
+    np.testing.assert_allclose(e_lse[live], lse[live], rtol=0, atol=1e-12)
+    assert np.all(eo[1] == 0) and np.all(ecor[1] == 0)
 
 
 def test_shift_v_shifts_output():

@@ -4,8 +4,10 @@ The oracle differentiates the explicit-Sigma definition with torch.autograd.
 These tests tie it to things other than itself: the pinned C oracle for the
 forward values, finite differences for the gradient, a library covariance for
 the exact rho gradient, the library softmax attention's own gradients at
-rho = 0, and two invariants of the definition. The last test checks the
-closed-form gradient that the GPU kernels stream against the oracle.
+rho = 0, and two invariants of the definition. The closed-form gradient that
+the GPU kernels stream, as the expanded oracle evaluates it densely for
+full-size checks, is checked against autograd through the explicit
+definition.
 """
 import math
 
@@ -15,6 +17,7 @@ import scipy.special
 import torch
 
 import oracle
+from oracle import expanded
 from oracle import grad as ograd
 
 
@@ -96,45 +99,15 @@ def test_shift_invariants_of_the_gradients():
     np.testing.assert_allclose(dv.sum(2).numpy(), want.numpy(), rtol=0, atol=1e-11)
 
 
-def _closed_form_grads(q, k, v, r, do):
-    """The gradient the kernels stream, dense in fp64. With w the causal
-    softmax weights, t = rho . k, sbar = sum_j w t, c = 1 + sbar - t,
-    u = dout . v, a = dout . o^SA and D = dout . o + a sbar:
-    dv_j = sum_i w c dout_i; dt = w (a - u); ds = w (c u + a t - D);
-    dq = tau ds K; dk = tau ds^T Q + dt^T R; drho = dt K."""
-    B, Hq, L, d = q.shape
-    G = Hq // k.shape[1]
-    kx, vx = (t.repeat_interleave(G, dim=1) for t in (k, v))
-    tau = 1.0 / math.sqrt(d)
-    causal = torch.ones(L, L, dtype=torch.bool).tril()
-    w = torch.softmax((tau * q @ kx.transpose(-1, -2)).masked_fill(~causal, -math.inf), -1)
-    t = r @ kx.transpose(-1, -2)
-    sbar = (w * t).sum(-1, keepdim=True)
-    c = 1.0 + sbar - t
-    osa = w @ vx
-    o = ((w * c) @ vx)
-    u = do @ vx.transpose(-1, -2)
-    a = (do * osa).sum(-1, keepdim=True)
-    D = (do * o).sum(-1, keepdim=True) + a * sbar
-    dt = w * (a - u)
-    ds = w * (c * u + a * t - D)
-    dvx = (w * c).transpose(-1, -2) @ do
-    dkx = tau * ds.transpose(-1, -2) @ q + dt.transpose(-1, -2) @ r
-    dq = tau * ds @ kx
-    dr = dt @ kx
-    fold = lambda x: x.reshape(B, Hq // G, G, L, d).sum(2)  # noqa: E731
-    return dq, fold(dkx), fold(dvx), dr, o
-
-
-@pytest.mark.parametrize("B,Hq,Hkv,L,d", [(1, 2, 1, 17, 4), (2, 4, 2, 40, 8)])
-def test_streamed_closed_form_matches_autograd(B, Hq, Hkv, L, d):
+@pytest.mark.parametrize("B,Hq,Hkv,L,d,block", [(1, 2, 1, 17, 4, 17), (2, 4, 2, 40, 8, 9)])
+def test_expanded_closed_form_matches_autograd(B, Hq, Hkv, L, d, block):
+    """The closed-form gradient of the expanded oracle (dense fp64, query rows
+    in blocks) against autograd through the explicit definition."""
     q, k, v, r, do = _inputs(B, Hq, Hkv, L, d, 7 + L)
     want = ograd.prefill_grad(q, k, v, r, do)
-    *got, o = _closed_form_grads(q, k, v, r, do)
-    np.testing.assert_allclose(o.numpy(), ograd.prefill_forward(q, k, v, r)[0].numpy(),
-                               rtol=0, atol=1e-12)
+    got = expanded.prefill_grad(q, k, v, r, do, row_block=block)
     for name, g_, w_ in zip("qkvr", got, want):
-        np.testing.assert_allclose(g_.numpy(), w_.numpy(), rtol=0, atol=1e-11, err_msg=name)
+        np.testing.assert_allclose(g_, w_.numpy(), rtol=0, atol=1e-11, err_msg=name)
 
 
 def test_row_and_key_gradients_match_the_full_gradient():

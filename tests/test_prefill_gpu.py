@@ -7,7 +7,7 @@ import oracle
 from parametrized_local_linear_gb300 import (PlxError, inputs, plx_check_device_error,
                                              plx_prefill_fwd, plx_prefill_fwd_f32)
 
-from helpers import assert_bf16_close, assert_f32_close, device, sample_rows
+from helpers import LSE_ABS, assert_bf16_close, assert_f32_close, device, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +55,7 @@ def test_bf16_small_matches_oracle_every_row(B, Hq, Hkv, L):
     out, lse = _run(plx_prefill_fwd, q, k, v, r)
     ref, ref_lse = oracle.prefill(q, k, v, r)
     assert_bf16_close(out.double().numpy(), ref, "out")
-    np.testing.assert_allclose(lse.double().numpy(), ref_lse, rtol=0, atol=2e-3)
+    np.testing.assert_allclose(lse.double().numpy(), ref_lse, rtol=0, atol=LSE_ABS)
 
 
 def test_bf16_large_probe_and_values():
@@ -84,7 +84,7 @@ def test_bf16_full_size_workload_sampled_rows(w):
     idx = tuple(torch.as_tensor(a) for a in np.array(rows).T)
     got = out[idx].double().numpy()
     assert_bf16_close(got, ref, w.name)
-    np.testing.assert_allclose(lse[idx].double().numpy(), ref_lse, rtol=0, atol=5e-3)
+    np.testing.assert_allclose(lse[idx].double().numpy(), ref_lse, rtol=0, atol=LSE_ABS)
     assert torch.isfinite(out).all(), "non-finite values in the full output"
 
 
@@ -125,7 +125,7 @@ def test_bf16_chunked_prefill_matches_oracle(B, Hq, Hkv, Lq, Lk):
     plx_check_device_error()
     ref, ref_lse = oracle.prefill(qc, k, v, rc)
     assert_bf16_close(out.double().cpu().numpy(), ref, "chunk")
-    np.testing.assert_allclose(lse.double().cpu().numpy(), ref_lse, rtol=0, atol=2e-3)
+    np.testing.assert_allclose(lse.double().cpu().numpy(), ref_lse, rtol=0, atol=LSE_ABS)
 
 
 def test_bf16_chunk_equals_tail_of_full_prefill_on_gpu():
