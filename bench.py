@@ -147,6 +147,65 @@ def whole_job_rate(world, units_per_rank_per_step, steps, max_ms):
     return world * units_per_rank_per_step * steps / (max_ms * 1e-3)
 
 
+def sharded_rate(units_per_step, steps, max_ms):
+    """Whole-job throughput when the ranks share one batch: every unit of the
+    batch was processed once, by one rank, and the job took the slowest
+    rank's time."""
+    return units_per_step * steps / (max_ms * 1e-3)
+
+
+# ---------------------------------------------------------------- sharding
+# The path partitions into independent (sequence, kv head) units: a kv head's
+# keys and values and the query heads that read them touch nothing else. With
+# --shard the ranks deal one batch's units among themselves, contiguous and
+# balanced, with no collective on the data path (each rank keeps its own
+# outputs).
+def shard_range(n_units, world, rank):
+    """Contiguous share [start, end) of n_units for `rank`: sizes differ by at
+    most one, the first n_units % world ranks taking the larger."""
+    base, extra = divmod(n_units, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
+def prefill_shard(B, Hkv, world, rank):
+    """The prefill units of `rank`: its contiguous range of the sequence-major
+    (sequence, kv head) list, cut at sequence boundaries into calls
+    (b, kv0, kv1), each one contiguous slice of the batch (sequence b, kv
+    heads kv0 .. kv1 - 1 and their query heads)."""
+    s, e = shard_range(B * Hkv, world, rank)
+    calls = []
+    u = s
+    while u < e:
+        b, kv0 = divmod(u, Hkv)
+        kv1 = min(Hkv, kv0 + (e - u))
+        calls.append((b, kv0, kv1))
+        u += kv1 - kv0
+    return calls
+
+
+def decode_shard(seqlens, world, rank):
+    """The decode sequences [b0, b1) of `rank`. The packed cache holds a
+    sequence's kv heads interleaved token by token, so a rank takes whole
+    sequences: contiguous ranges whose ends are the first sequence boundaries
+    at or past k / world of the batch's cached tokens (k = 1 .. world - 1),
+    so cached tokens, the decode's work, spread as evenly as whole sequences
+    allow."""
+    lens = [max(0, int(x)) for x in seqlens]
+    cum = [0]
+    for n in lens:
+        cum.append(cum[-1] + n)
+    total = cum[-1]
+
+    def cut(k):
+        if k >= world:
+            return len(lens)
+        goal = total * k / world
+        return next(i for i, c in enumerate(cum) if c >= goal)
+
+    return cut(rank), cut(rank + 1)
+
+
 def oracle_prefill_sample(w, q, k, v, r, budget_s, seed, threads=None):
     """Time the fp64 oracle on seeded random causal rows of workload w until
     about budget_s seconds of oracle time; return (algorithmic flops of the
@@ -215,6 +274,79 @@ def oracle_extra_samples(w, q, k, v, r, budget_s, seed=12):
         "value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
         "kind": "oracle", "sample": f"{n} token rows (numpy fp64 product), {secs:.1f} s"}
     return out
+
+
+def cpu_baseline_plan(dev, explicit_budget_s=4.0, seed=21):
+    """The CPU oracles timed on each of the five workloads, on this host's
+    cores: the explicit-Sigma C oracle (configs 1, 4, 5 on the whole workload
+    or a stated sample of it; configs 2, 3 on random rows, extrapolated by
+    pair count) and the expanded fp64 form on the whole workload. Inputs are
+    the same distributions, drawn on the device and copied to the host; the
+    copies are not timed. Returns {workload: {oracle: result}}."""
+    import random
+
+    import oracle
+    from oracle import expanded
+    rng = random.Random(seed)
+    threads = oracle.default_threads()
+    tthreads = torch.get_num_threads()
+    res = {}
+
+    def timed(fn):
+        ts = time.perf_counter()
+        fn()
+        return time.perf_counter() - ts
+
+    # Config 1: the whole tiny fp32 prefill, both oracles.
+    w = inputs.TINY_PREFILL_F32
+    q, k, v, r = inputs.prefill_inputs_for(w)
+    t_exp = timed(lambda: oracle.prefill(q, k, v, r, threads=threads))
+    t_dense = timed(lambda: expanded.prefill(q, k, v, r))
+    res[w.name] = {
+        "explicit": {"value": w.flops / t_exp / 1e12, "unit": "TFLOP/s", "seconds": t_exp,
+                     "cores": threads, "sample": "whole workload"},
+        "expanded": {"value": w.flops / t_dense / 1e12, "unit": "TFLOP/s", "seconds": t_dense,
+                     "cores": tthreads, "sample": "whole workload"}}
+    # Configs 2, 3: explicit on random rows, extrapolated; expanded in full.
+    for w in (inputs.PREFILL_0P6B, inputs.PREFILL_1P7B):
+        q, k, v, r = (t.cpu() for t in inputs.prefill_inputs_for(w, device=dev))
+        f, secs, rows, _ = oracle_prefill_sample(w, q, k, v, r, explicit_budget_s,
+                                                 seed=rng.randrange(1 << 30), threads=threads)
+        t_dense = timed(lambda: expanded.prefill(q, k, v, r))
+        res[w.name] = {
+            "explicit": {"value": f / secs / 1e12, "unit": "TFLOP/s", "seconds": secs,
+                         "cores": threads, "extrapolated_full_s": w.flops / (f / secs),
+                         "sample": f"{rows} random causal rows, extrapolated by pair count"},
+            "expanded": {"value": w.flops / t_dense / 1e12, "unit": "TFLOP/s",
+                         "seconds": t_dense, "cores": tthreads, "sample": "whole workload"}}
+        del q, k, v, r
+    # Configs 4, 5: explicit on whole (sequence, head) pairs until the budget
+    # is spent, reported per pair and as the cache rate it implies for the
+    # whole batch; expanded in full.
+    for w in (inputs.DECODE_B64, inputs.DECODE_RAGGED):
+        q, r, kc, vc, sl = inputs.decode_inputs_for(w, device=dev)
+        q, r, kc, vc = (t.cpu() for t in (q, r, kc, vc))
+        lens = sl.tolist()
+        pairs, secs, keys = 0, 0.0, 0
+        while secs < explicit_budget_s:
+            batch = [(rng.randrange(w.B), rng.randrange(w.Hq)) for _ in range(threads)]
+            secs += timed(lambda: oracle.decode(q, r, kc, vc, sl, pairs=batch, threads=threads))
+            pairs += len(batch)
+            keys += sum(lens[b] for b, _ in batch)
+        full_keys = sum(lens) * w.Hq
+        full_s = secs * full_keys / keys
+        by = w.bytes_moved()
+        t_dense = timed(lambda: expanded.decode(q, r, kc, vc, sl))
+        res[w.name] = {
+            "explicit": {"value": by / full_s / 1e9, "unit": "GB/s", "seconds": secs,
+                         "cores": threads, "pairs_per_s": pairs / secs,
+                         "extrapolated_full_s": full_s,
+                         "sample": f"{pairs} random (sequence, head) pairs, extrapolated by "
+                                   "cached keys"},
+            "expanded": {"value": by / t_dense / 1e9, "unit": "GB/s", "seconds": t_dense,
+                         "cores": tthreads, "sample": "whole workload"}}
+        del q, r, kc, vc
+    return res
 
 
 def run_reference(args, world, rank):
@@ -303,6 +435,9 @@ def main():
     ap.add_argument("--impl", default="plx", choices=["plx", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the 1.7B / ragged timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shard", action="store_true",
+                    help="under torchrun, deal one batch's (sequence, kv head) units among the "
+                         "ranks (strong scaling) instead of a full replica per rank")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_ragged", "decode_long", "backward",
                                            "projection"], default=None,
@@ -333,15 +468,43 @@ def main():
     out = torch.empty_like(q)
     lse = torch.empty(wp.B, wp.Hq, wp.L, device=dev)
     dq, dr, kc, vc, sl = inputs.decode_inputs_for(wd, device=dev)
+    lens = sl.tolist()
     sl = sl.to(dev)
     dout = torch.empty_like(dq)
     dbytes = wd.bytes_moved()
+    G = wp.Hq // wp.Hkv
+    # This rank's prefill calls (b, kv0, kv1) and decode sequences [b0, b1):
+    # with --shard its share of the one batch; otherwise (replicas) the whole
+    # batch, whose timed prefill is one batched call and whose end-to-end leg
+    # calls the prefill once per sequence.
+    if args.shard:
+        pcalls = prefill_shard(wp.B, wp.Hkv, world, rank)
+        b0, b1 = decode_shard(lens, world, rank)
+    else:
+        pcalls = [(b, 0, wp.Hkv) for b in range(wp.B)]
+        b0, b1 = 0, wd.B
+    t0, t1 = sum(lens[:b0]), sum(lens[:b1])
+    own_flops = sum(8 * wp.d * (c[2] - c[1]) * G * wp.L * (wp.L + 1) // 2 for c in pcalls)
+    own_dbytes = (2 * (t1 - t0) * wd.Hkv * wd.d + 3 * (b1 - b0) * wd.Hq * wd.d) * 2
+
+    def pviews(b, kv0, kv1, ts=(q, k, v, r, out, lse)):
+        qq, kk, vv, rr, oo, ll = ts
+        h0, h1 = kv0 * G, kv1 * G
+        return (qq[b:b + 1, h0:h1], kk[b:b + 1, kv0:kv1], vv[b:b + 1, kv0:kv1], rr[b:b + 1, h0:h1],
+                oo[b:b + 1, h0:h1], ll[b:b + 1, h0:h1])
+
+    dviews = (dq[b0:b1], dr[b0:b1], kc[t0:t1], vc[t0:t1], sl[b0:b1], dout[b0:b1])
 
     def step(ev):
         ev[0].record(stream)
-        plx_prefill_fwd(q, k, v, r, out, lse)
+        if args.shard:
+            for c in pcalls:
+                plx_prefill_fwd(*pviews(*c))
+        else:
+            plx_prefill_fwd(q, k, v, r, out, lse)
         ev[1].record(stream)
-        plx_decode_fwd(dq, dr, kc, vc, sl, dout)
+        if b1 > b0:
+            plx_decode_fwd(*dviews)
         ev[2].record(stream)
 
     for _ in range(args.warmup):
@@ -374,10 +537,17 @@ def main():
     dec_ms_max = max_over_ranks(dec_ms, world, dev)
     total_ms_max = max_over_ranks(total_ms, world, dev)
     K = args.steps
-    value = whole_job_rate(world, wp.flops, K, pre_ms_max) / 1e12
-    dec_gbs = whole_job_rate(world, dbytes, K, dec_ms_max) / 1e9
+    if args.shard:
+        value = sharded_rate(wp.flops, K, pre_ms_max) / 1e12
+        dec_gbs = sharded_rate(dbytes, K, dec_ms_max) / 1e9
+    else:
+        value = whole_job_rate(world, wp.flops, K, pre_ms_max) / 1e12
+        dec_gbs = whole_job_rate(world, dbytes, K, dec_ms_max) / 1e9
+    # Per-launch rates of this rank's own work (rank 0 prints them).
     pre_launch_s = pre_ms / K * 1e-3
     dec_launch_s = dec_ms / K * 1e-3
+    pre_launch_flops = wp.flops if not args.shard else own_flops
+    dec_launch_bytes = dbytes if not args.shard else own_dbytes
     tc_peak = _peak(peaks, "bf16_tflops")
     hbm_peak = _peak(peaks, "hbm_gbs")
 
@@ -396,24 +566,31 @@ def main():
     # the critical path.
     hq = [t.cpu().pin_memory() for t in (q, k, v, r)]
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    hd = [t.cpu().pin_memory() for t in (dq, dr)]
-    hdout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in hq + hd)
-    d2h = hout.numel() * hout.element_size() + hdout.numel() * hdout.element_size()
-    nseq = q.shape[0]
+    hd = [t[b0:b1].cpu().pin_memory() for t in (dq, dr)]
+    hdout = torch.empty(dout[b0:b1].shape, dtype=dout.dtype).pin_memory()
+
+    def hviews(b, kv0, kv1):
+        h0, h1 = kv0 * G, kv1 * G
+        return (hq[0][b:b + 1, h0:h1], hq[1][b:b + 1, kv0:kv1], hq[2][b:b + 1, kv0:kv1],
+                hq[3][b:b + 1, h0:h1])
+
+    nbytes = lambda t: t.numel() * t.element_size()  # noqa: E731
+    h2d = sum(nbytes(t) for c in pcalls for t in hviews(*c)) + sum(nbytes(t) for t in hd)
+    d2h = sum(nbytes(pviews(*c)[4]) for c in pcalls) + nbytes(hdout)
     copy_stream = torch.cuda.Stream(dev)
-    dseq = [[torch.empty_like(t[b:b + 1]) for t in (q, k, v, r)] for b in range(nseq)]
-    dseq_out = [torch.empty_like(out[b:b + 1]) for b in range(nseq)]
-    ddec = [torch.empty_like(t) for t in (dq, dr)]
-    ddec_out = torch.empty_like(dout)
+    dseq = [[torch.empty_like(t, device=dev) for t in hviews(*c)] for c in pcalls]
+    dseq_out = [torch.empty_like(pviews(*c)[4]) for c in pcalls]
+    ddec = [torch.empty_like(t, device=dev) for t in hd]
+    ddec_out = torch.empty_like(hdout, device=dev)
+    hout_views = [pviews(*c, ts=(hq[0], hq[1], hq[2], hq[3], hout, hout))[4] for c in pcalls]
 
     def e2e_step():
         ev_in = []
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_stream(stream)  # the previous step is done with the buffers
-            for b in range(nseq):
-                for dst, src in zip(dseq[b], hq):
-                    dst.copy_(src[b:b + 1], non_blocking=True)
+            for c, dst_c in zip(pcalls, dseq):
+                for dst, src in zip(dst_c, hviews(*c)):
+                    dst.copy_(src, non_blocking=True)
                 ev_in.append(torch.cuda.Event())
                 ev_in[-1].record(copy_stream)
             for dst, src in zip(ddec, hd):
@@ -421,19 +598,20 @@ def main():
             ev_dec = torch.cuda.Event()
             ev_dec.record(copy_stream)
         ev_out = []
-        for b in range(nseq):
-            stream.wait_event(ev_in[b])
-            plx_prefill_fwd(*dseq[b], dseq_out[b])
+        for n in range(len(pcalls)):
+            stream.wait_event(ev_in[n])
+            plx_prefill_fwd(*dseq[n], dseq_out[n])
             ev_out.append(torch.cuda.Event())
             ev_out[-1].record(stream)
         stream.wait_event(ev_dec)
-        plx_decode_fwd(ddec[0], ddec[1], kc, vc, sl, ddec_out)
+        if b1 > b0:
+            plx_decode_fwd(ddec[0], ddec[1], kc[t0:t1], vc[t0:t1], sl[b0:b1], ddec_out)
         ev_d = torch.cuda.Event()
         ev_d.record(stream)
         with torch.cuda.stream(copy_stream):
-            for b in range(nseq):
-                copy_stream.wait_event(ev_out[b])
-                hout[b:b + 1].copy_(dseq_out[b], non_blocking=True)
+            for n in range(len(pcalls)):
+                copy_stream.wait_event(ev_out[n])
+                hout_views[n].copy_(dseq_out[n], non_blocking=True)
             copy_stream.wait_event(ev_d)
             hdout.copy_(ddec_out, non_blocking=True)
         stream.wait_stream(copy_stream)
@@ -443,21 +621,26 @@ def main():
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
     ke = max(3, min(K, 10))
+    barrier(world)
     e0.record(stream)
     for _ in range(ke):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / ke
-    # Per-sequence calls give bit-for-bit the batched call's output.
-    if not torch.equal(hout, out.cpu()):
-        raise RuntimeError("e2e prefill output differs from the batched call")
+    # The slices called separately give bit for bit the batched call's output.
+    for c, hv in zip(pcalls, hout_views):
+        if not torch.equal(hv, pviews(*c)[4].cpu()):
+            raise RuntimeError(f"e2e prefill output of call {c} differs from the batched call")
     # The e2e step also contains the decode; count its time, credit only prefill flops.
-    e2e_value = world * wp.flops / (e2e_ms * 1e-3) / 1e12
+    if args.shard:
+        e2e_value = wp.flops / (e2e_ms * 1e-3) / 1e12
+    else:
+        e2e_value = world * wp.flops / (e2e_ms * 1e-3) / 1e12
 
     # ---------------------------------------------------------------- extra
     extra = {}
-    if not args.no_extra:
+    if not args.no_extra and not args.shard:
         del hq, hd
         from parametrized_local_linear_gb300 import (plx_decode_fwd_cor, plx_prefill_fwd_chunk,
                                                      plx_prefill_fwd_cor)
@@ -592,8 +775,8 @@ def main():
         plx_check_device_error()
 
     # ---------------------------------------------------------------- cpu baseline
-    cpu = None
-    if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
+    cpu, cpu_plan = None, None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
         import oracle
         oracle.build()
         f, secs, rows, threads = oracle_prefill_sample(wp, q, k, v, r, args.cpu_seconds, seed=11)
@@ -604,6 +787,7 @@ def main():
             for name, base in oracle_extra_samples(wp, q, k, v, r, args.cpu_seconds / 4).items():
                 if name in extra:
                     extra[name]["cpu_baseline"] = base
+        cpu_plan = cpu_baseline_plan(dev, explicit_budget_s=args.cpu_seconds / 3)
 
     clocks = clk.summary()
     line = {
@@ -615,36 +799,40 @@ def main():
         "warmup": args.warmup,
         "ms_per_step": total_ms_max / K,
         "higher_is_better": True,
-        "scaling": "weak",
+        "scaling": "strong" if args.shard else "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": wp.name, "decode_workload": wd.name,
                    "step": "prefill 0.6B-shaped + decode B64 ctx8192",
                    "l2": "inputs larger than L2 (prefill 256 MB, decode 2.1 GB); no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": (f"one batch sharded over (sequence, kv head) units x{world}"
+                                   if args.shard else
+                                   f"replicas x{world}" if world > 1 else "single GPU")},
         "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel",
-                     "achieved": wp.flops / pre_launch_s / 1e12, "peak": tc_peak,
-                     "unit": "TFLOP/s", "frac": wp.flops / pre_launch_s / 1e12 / tc_peak,
+                     "achieved": pre_launch_flops / pre_launch_s / 1e12, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": pre_launch_flops / pre_launch_s / 1e12 / tc_peak,
                      "peak_source": f"bf16_tflops ({'of measured' if peaks_src == 'measured' else 'of fallback'})",
                      "traffic": NCU_TRAFFIC_BYTES["prefill_tc_kernel"],
-                     "algorithmic_flops_per_launch": wp.flops},
+                     "algorithmic_flops_per_launch": pre_launch_flops},
         "decode": {"workload": wd.name, "value": dec_gbs, "unit": "GB/s",
                    "ms": dec_launch_s * 1e3,
                    "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + combine",
-                                "achieved": dbytes / dec_launch_s / 1e9, "peak": hbm_peak,
-                                "unit": "GB/s", "frac": dbytes / dec_launch_s / 1e9 / hbm_peak,
+                                "achieved": dec_launch_bytes / dec_launch_s / 1e9,
+                                "peak": hbm_peak, "unit": "GB/s",
+                                "frac": dec_launch_bytes / dec_launch_s / 1e9 / hbm_peak,
                                 "peak_source": f"hbm_gbs ({peaks_src})",
                                 "traffic": NCU_TRAFFIC_BYTES["decode_split_kernel"],
-                                "algorithmic_bytes_per_launch": dbytes}},
+                                "algorithmic_bytes_per_launch": dec_launch_bytes}},
         "extra": extra,
         "cpu_baseline": cpu,
+        "cpu_baselines": cpu_plan,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "method": "one prefill call per sequence; host copies on a second stream, "
                           "overlapped with the kernels, inside the timing; the host link "
                           "(about 210 GB/s up, 192 GB/s down) bounds it"},
-        "gpu_launches": 3 * K,
+        "gpu_launches": K * ((len(pcalls) if args.shard else 1) + (2 if b1 > b0 else 0)),
         "clocks": clocks,
         "gpu": torch.cuda.get_device_name(dev),
     }
