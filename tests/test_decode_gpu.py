@@ -50,11 +50,12 @@ def _share_invariance_bound(q, r, kc, vc, lens, base):
 
     A share count moves the running max each CTA exponentiates against, and
     so the bf16 rounding of every weight p_j and product p_j t_j that enters
-    the value products (relative error at most 2^-9 each, for either run).
+    the value products (relative error at most 2^-8 each, for either run:
+    bf16 keeps 8 significant bits, rounded to nearest).
     With w the normalised weights, t_j = rho . k_j and s = sum_j w_j t_j, one
     run's O1 = sum w v and O2 = sum w t v then move by at most
-    2^-9 sum_j w_j |v_j| and 2^-9 sum_j w_j |t_j v_j| per element, and
-    o = O1 (1 + s) - O2 by at most 2^-9 ((1 + |s|) sum w |v| + sum w |t v|);
+    2^-8 sum_j w_j |v_j| and 2^-8 sum_j w_j |t_j v_j| per element, and
+    o = O1 (1 + s) - O2 by at most 2^-8 ((1 + |s|) sum w |v| + sum w |t v|);
     two runs double that. Each output is rounded to bf16 once (half an ulp
     each, one ulp together); fp32 summation order adds far less."""
     B, Hq, d = q.shape
@@ -69,7 +70,7 @@ def _share_invariance_bound(q, r, kc, vc, lens, base):
             w = torch.softmax(Kh @ q[b, h].double() / np.sqrt(d), dim=0)
             t = Kh @ r[b, h].double()
             s = float((w * t).sum())
-            bound[b, h] = 2 * 2.0 ** -9 * ((1 + abs(s)) * (w @ Vh.abs()) + w @ (t.abs()[:, None] * Vh.abs())).numpy()
+            bound[b, h] = 2 * 2.0 ** -8 * ((1 + abs(s)) * (w @ Vh.abs()) + w @ (t.abs()[:, None] * Vh.abs())).numpy()
     mag = np.abs(base.double().numpy())
     ulp = np.where(mag > 0, 2.0 ** (np.floor(np.log2(np.where(mag > 0, mag, 1.0))) - 7), 2.0 ** -133)
     return bound + ulp
@@ -173,7 +174,7 @@ def test_decode_all_sequences_empty():
 ])
 def test_decode_cor_matches_oracle(lens, Hq, Hkv):
     from parametrized_local_linear_gb300 import plx_decode_fwd_cor
-    from helpers import assert_cor_close
+    from helpers import assert_cor_close, cor_bounds_decode
     dev = device()
     q, r, kc, vc, sl = inputs.decode_inputs(len(lens), Hq, Hkv, 128, lens, torch.bfloat16, 0.05,
                                             2 * len(lens) + Hq)
@@ -184,7 +185,7 @@ def test_decode_cor_matches_oracle(lens, Hq, Hkv):
     plx_check_device_error()
     assert torch.equal(out, plain)  # the side output leaves o untouched
     _, _, ref = oracle.decode(q, r, kc, vc, sl, with_cor=True)
-    assert_cor_close(cor.cpu().numpy(), ref, "decode cor")
+    assert_cor_close(cor.cpu().numpy(), ref, cor_bounds_decode(q, r, kc, vc, sl), "decode cor")
     for b, n in enumerate(lens):
         if n == 0:
             assert torch.all(cor[b] == 0)  # no keys: o = 0 and the ratio is defined as 0
