@@ -483,9 +483,9 @@ def main():
     else:
         pcalls = [(b, 0, wp.Hkv) for b in range(wp.B)]
         b0, b1 = 0, wd.B
-    t0, t1 = sum(lens[:b0]), sum(lens[:b1])
+    tok0, tok1 = sum(lens[:b0]), sum(lens[:b1])
     own_flops = sum(8 * wp.d * (c[2] - c[1]) * G * wp.L * (wp.L + 1) // 2 for c in pcalls)
-    own_dbytes = (2 * (t1 - t0) * wd.Hkv * wd.d + 3 * (b1 - b0) * wd.Hq * wd.d) * 2
+    own_dbytes = (2 * (tok1 - tok0) * wd.Hkv * wd.d + 3 * (b1 - b0) * wd.Hq * wd.d) * 2
 
     def pviews(b, kv0, kv1, ts=(q, k, v, r, out, lse)):
         qq, kk, vv, rr, oo, ll = ts
@@ -493,7 +493,7 @@ def main():
         return (qq[b:b + 1, h0:h1], kk[b:b + 1, kv0:kv1], vv[b:b + 1, kv0:kv1], rr[b:b + 1, h0:h1],
                 oo[b:b + 1, h0:h1], ll[b:b + 1, h0:h1])
 
-    dviews = (dq[b0:b1], dr[b0:b1], kc[t0:t1], vc[t0:t1], sl[b0:b1], dout[b0:b1])
+    dviews = (dq[b0:b1], dr[b0:b1], kc[tok0:tok1], vc[tok0:tok1], sl[b0:b1], dout[b0:b1])
 
     def step(ev):
         ev[0].record(stream)
@@ -605,7 +605,7 @@ def main():
             ev_out[-1].record(stream)
         stream.wait_event(ev_dec)
         if b1 > b0:
-            plx_decode_fwd(ddec[0], ddec[1], kc[t0:t1], vc[t0:t1], sl[b0:b1], ddec_out)
+            plx_decode_fwd(ddec[0], ddec[1], kc[tok0:tok1], vc[tok0:tok1], sl[b0:b1], ddec_out)
         ev_d = torch.cuda.Event()
         ev_d.record(stream)
         with torch.cuda.stream(copy_stream):

@@ -26,8 +26,9 @@
 //     S = Q K^T, T = R K^T, U = dO V^T; dS, dT; dQ += dS K, dR += dT K.
 //   bwd_dkv_kernel: one CTA per 128 keys of one kv head, over every query
 //     head of its group and every 64-query tile at or after the keys;
-//     S^T = K Q^T, T^T = K R^T, U^T = V dO^T; then dV += (w c)^T dO and
-//     dK += dS^T Q + dT^T R.
+//     [S^T | T^T] = K [Q; R]^T (one N = 128 product: S^T and T^T share the
+//     A operand K, so stacking Q and R reads K once per K step) and
+//     U^T = V dO^T; then dV += (w c)^T dO and dK += dS^T Q + dT^T R.
 // Neither kernel needs atomics: each output row is owned by one CTA. The
 // elementwise warps release S, T and U as soon as they have loaded them
 // (stu_free), so the next tile's score UMMAs run under the elementwise work
@@ -430,7 +431,11 @@ constexpr int NST = 3;                         // Q / R / dO ring stages
 constexpr int HALF_K = BM * 64 * 2;            // 16 KB
 constexpr int HALF_Q = BN * 64 * 2;            // 8 KB
 constexpr int TILE_Q = 2 * HALF_Q;             // 16 KB
-constexpr int STAGE = 3 * TILE_Q;              // Q, R, dO
+// A stage holds the 64 queries' Q, R and dO as [Q h0 | R h0 | Q h1 | R h1 |
+// dO h0 | dO h1] (h0, h1: dims 0-63 and 64-127): within each half Q's rows
+// are followed by R's, so [Q; R] is one K-major operand of 128 rows and
+// S^T and T^T come from one N = 128 product that reads K once.
+constexpr int STAGE = 3 * TILE_Q;
 constexpr int OFF_K = 0, OFF_V = 2 * HALF_K;
 constexpr int OFF_P = 4 * HALF_K;              // 65536: (w c)^T tile, 128 keys x 64 queries bf16
 constexpr int OFF_STG = OFF_P + BM * BN * 2;   // 81920
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&q_full[s]), 1);
       mbar_init(smem_u32(&q_empty[s]), 2);
     }
-    mbar_init(smem_u32(stu_full), 3);
+    mbar_init(smem_u32(stu_full), 2);  // [S^T | T^T] and U^T
     mbar_init(smem_u32(stu_free), NEW);
     mbar_init(smem_u32(gs_full), NEW);
     mbar_init(smem_u32(acc_done), 2);
@@ -521,9 +526,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t base = smem_u32(smem + OFF_STG + st * STAGE);
         mbar_arrive_expect_tx(qf, STAGE);
         tma_load_3d(base, &tm_q, 0, y, zq, qf);
-        tma_load_3d(base + HALF_Q, &tm_q, 64, y, zq, qf);
-        tma_load_3d(base + TILE_Q, &tm_r, 0, y, zq, qf);
-        tma_load_3d(base + TILE_Q + HALF_Q, &tm_r, 64, y, zq, qf);
+        tma_load_3d(base + HALF_Q, &tm_r, 0, y, zq, qf);
+        tma_load_3d(base + 2 * HALF_Q, &tm_q, 64, y, zq, qf);
+        tma_load_3d(base + 3 * HALF_Q, &tm_r, 64, y, zq, qf);
         tma_load_3d(base + 2 * TILE_Q, &tm_do, 0, y, zq, qf);
         tma_load_3d(base + 2 * TILE_Q + HALF_Q, &tm_do, 64, y, zq, qf);
         issued = s + 1;
@@ -537,18 +542,27 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < EW_WARP0) {
     if (lane == 0) {
       // ---------------------------------------------------------- UMMA issuers
-      // role 0: S^T = K Q^T and dV += (w c)^T dO; role 1: T^T = K R^T and
+      // role 0: [S^T | T^T] = K [Q; R]^T (one N = 128 product; its columns
+      // are S^T [0, 64) and T^T [64, 128)) and dV += (w c)^T dO; role 1:
       // dK += (tau dS)^T Q + dT^T R (one thread, so the accumulator's first
       // write comes first); role 2: U^T = V dO^T.
       const int role = warp - 1;
-      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
+      const bool scores = role != 1;
+      constexpr uint32_t idesc_st = idesc_bf16_f32(BM, 2 * BN, 0);
+      constexpr uint32_t idesc_u = idesc_bf16_f32(BM, BN, 0);
       constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, 1);
       const uint64_t adesc = smem_desc_sw128(smem_u32(smem + (role == 2 ? OFF_V : OFF_K)), 16, 1024);
       const uint64_t pdesc = smem_desc_sw128(smem_u32(smem + OFF_P), 16, 1024);
-      // Stage operand `role` (Q, R, dO) in its K-major and MN-major views.
-      const uint64_t stg_k = smem_desc_sw128(smem_u32(smem + OFF_STG + role * TILE_Q), 16, 1024);
-      const uint64_t stg_mn = smem_desc_sw128(smem_u32(smem + OFF_STG), HALF_Q, 1024);
-      const uint32_t dcol = tbase + (role == 0 ? COL_S : role == 1 ? COL_T : COL_U);
+      // The score operand in K-major view: [Q; R] (128 rows, dim halves
+      // 2 HALF_Q apart) for role 0, dO (64 rows, halves HALF_Q apart) for
+      // role 2. MN-major views for the gradients: Q and R (halves 2 HALF_Q
+      // apart), dO (HALF_Q apart).
+      const uint64_t stg_k = smem_desc_sw128(smem_u32(smem + OFF_STG + (role == 2 ? 2 * TILE_Q : 0)), 16, 1024);
+      const uint32_t slab = role == 2 ? (HALF_Q >> 4) : (2 * HALF_Q >> 4);
+      const uint64_t qr_mn = smem_desc_sw128(smem_u32(smem + OFF_STG), 2 * HALF_Q, 1024);
+      const uint64_t do_mn = smem_desc_sw128(smem_u32(smem + OFF_STG + 2 * TILE_Q), HALF_Q, 1024);
+      const uint32_t dcol = tbase + (role == 2 ? COL_U : COL_S);
+      const uint32_t idesc_s = role == 2 ? idesc_u : idesc_st;
       bool ok = mbar_wait(smem_u32(kv_full), 0, ab);
       auto issue_score = [&](int s) -> bool {
         const int st = s % NST;
@@ -558,21 +572,24 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           umma_ss(dcol, adesc + (ks >> 2) * (HALF_K >> 4) + (ks & 3) * 2,
-                  bd + (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2, idesc_s, ks > 0);
+                  bd + (ks >> 2) * slab + (ks & 3) * 2, idesc_s, ks > 0);
         umma_commit(smem_u32(stu_full));
         return true;
       };
-      ok = ok && issue_score(0);
+      if (scores) ok = ok && issue_score(0);
       for (int s = 0; ok && s < n; ++s) {
-        if (s + 1 < n) {
+        if (scores && s + 1 < n) {
           if (!mbar_wait(smem_u32(stu_free), s & 1, ab) || !issue_score(s + 1)) break;
         }
         if (role == 2) continue;
         if (!mbar_wait(smem_u32(gs_full), s & 1, ab)) break;
-        tc_fence_after();
         const int st = s % NST;
-        const uint64_t qm = stg_mn + st * (STAGE >> 4);
-        const uint64_t rm = qm + (TILE_Q >> 4), om = qm + 2 * (TILE_Q >> 4);
+        // The stage's loads completed before its score products ran (role 0
+        // waited on q_full); role 1 observes that too before reading Q and R.
+        if (!scores && !mbar_wait(smem_u32(&q_full[st]), (s / NST) & 1, ab)) break;
+        tc_fence_after();
+        const uint64_t qm = qr_mn + st * (STAGE >> 4);
+        const uint64_t rm = qm + (HALF_Q >> 4), om = do_mn + st * (STAGE >> 4);
         if (role == 0) {
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
