@@ -306,10 +306,9 @@ int plx_decode_default_nsplit(int B, int Hkv) {
 
 namespace {
 
-plx_status decode_bf16(const char *fn, const void *q, const void *r, const void *kcache,
-                       const void *vcache, const int *seqlens, void *out, float *cor, int B,
-                       int Hq, int Hkv, int d, int nsplit, bool default_share, void *workspace,
-                       size_t workspace_bytes, void *stream) {
+plx_status check_decode_args(const char *fn, const void *q, const void *r, const void *kcache,
+                             const void *vcache, const int *seqlens, void *out, int B, int Hq,
+                             int Hkv, int d) {
   if (!q || !r || !kcache || !vcache || !seqlens || !out)
     return fail(PLX_ERR_INVALID_ARG, "%s: null pointer", fn);
   plx_status s = check_common(fn, B, Hq, Hkv, 1, d);
@@ -320,6 +319,15 @@ plx_status decode_bf16(const char *fn, const void *q, const void *r, const void 
     return fail(PLX_ERR_UNSUPPORTED, "%s: B * Hq must be <= 2^24", fn);
   if (!aligned16(q) || !aligned16(r) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
     return fail(PLX_ERR_INVALID_ARG, "%s: tensor pointers must be 16-byte aligned", fn);
+  return PLX_OK;
+}
+
+plx_status decode_bf16(const char *fn, const void *q, const void *r, const void *kcache,
+                       const void *vcache, const int *seqlens, void *out, float *cor, int B,
+                       int Hq, int Hkv, int d, int nsplit, bool default_share, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+  plx_status s = check_decode_args(fn, q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, d);
+  if (s) return s;
   if (nsplit < 1) return fail(PLX_ERR_INVALID_ARG, "%s: nsplit %d", fn, nsplit);
   if (nsplit > 65535) return fail(PLX_ERR_INVALID_ARG, "%s: nsplit %d too large", fn, nsplit);
   const size_t need = plx::decode_workspace_bytes(B, Hq, Hkv, d, nsplit);
@@ -376,14 +384,16 @@ plx_status plx_decode_fwd_noalloc(const void *q, const void *r, const void *kcac
                                   int Hkv, int d, void *stream) {
   const char *fn = "plx_decode_fwd_noalloc";
   const size_t cap_bytes = plx::kNoAllocScratchFloats * sizeof(float);
-  if (B >= 1 && Hq >= 1 && Hkv >= 1 && d >= 1 && Hq % Hkv == 0) {
-    const size_t one = plx_decode_workspace_bytes(B, Hq, Hkv, d, 1);
-    if (one > cap_bytes)
-      return fail(PLX_ERR_UNSUPPORTED,
-                  "%s: B * Hq = %lld needs %zu bytes of records even with one CTA; "
-                  "the fixed array holds %zu bytes (use plx_decode_fwd)",
-                  fn, static_cast<long long>(B) * Hq, one, cap_bytes);
-  }
+  // Arguments are checked before the array's address is looked up, so a
+  // rejected call makes no CUDA call at all.
+  plx_status s = check_decode_args(fn, q, r, kcache, vcache, seqlens, out, B, Hq, Hkv, d);
+  if (s) return s;
+  const size_t one = plx_decode_workspace_bytes(B, Hq, Hkv, d, 1);
+  if (one > cap_bytes)
+    return fail(PLX_ERR_UNSUPPORTED,
+                "%s: B * Hq = %lld needs %zu bytes of records even with one CTA; "
+                "the fixed array holds %zu bytes (use plx_decode_fwd)",
+                fn, static_cast<long long>(B) * Hq, one, cap_bytes);
   float *scratch = nullptr;
   cudaError_t e = plx::noalloc_scratch(&scratch);
   if (e != cudaSuccess) return cuda_fail(e, "plx_decode_fwd_noalloc: scratch address");

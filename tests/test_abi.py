@@ -127,3 +127,17 @@ def test_backward_and_projection_reject_bad_arguments(lib):
     assert b"multiple of 8" in lib.plx_last_error_message()
     assert proj(p, p, p, p, p, p, 1, 16, 128, 2, 1, 64, None) == binding.PLX_ERR_UNSUPPORTED
     assert proj(p, p, None, p, p, p, 1, 16, 128, 2, 1, 128, None) == binding.PLX_ERR_INVALID_ARG
+
+
+def test_noalloc_decode_rejects_bad_arguments_before_any_cuda_call(lib):
+    """The allocation-free decode checks its arguments before it looks up its
+    fixed array's device address: on a host without a GPU a bad call still
+    gets the argument error, not a CUDA error."""
+    p = ctypes.c_void_p(4096)
+    f = lib.plx_decode_fwd_noalloc
+    assert f(None, p, p, p, p, p, 2, 4, 2, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert b"null" in lib.plx_last_error_message()
+    assert f(p, p, p, p, p, p, 2, 32, 2, 128, None) == binding.PLX_ERR_UNSUPPORTED  # 16 a kv head
+    assert f(p, p, p, p, p, p, 2, 4, 2, 64, None) == binding.PLX_ERR_UNSUPPORTED
+    assert f(p, p, p, p, p, ctypes.c_void_p(4100), 2, 4, 2, 128, None) == binding.PLX_ERR_INVALID_ARG
+    assert b"aligned" in lib.plx_last_error_message()
