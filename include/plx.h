@@ -53,6 +53,7 @@ typedef int plx_status;
 #define PLX_ERR_UNSUPPORTED 2    /* valid but not implemented (e.g. head dim) */
 #define PLX_ERR_CUDA 3           /* a CUDA runtime or driver call failed */
 #define PLX_ERR_DEVICE_TIMEOUT 4 /* a bounded in-kernel wait ran out */
+#define PLX_ERR_BOUNDS 5         /* a device-side index check failed (debug build only) */
 
 /*
  * Causal prefill, bf16 in / bf16 out, fp32 accumulation (tcgen05 tensor cores).
@@ -261,8 +262,20 @@ int plx_decode_default_nsplit(int B, int Hkv);
  * PLX_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the last check,
  * PLX_ERR_INVALID_ARG if a kernel found its device-side inputs out of range
  * (decode lengths summing to 2^30 tokens or more; that call did no work and
- * its outputs are undefined), PLX_ERR_CUDA if the stream reports an error,
- * else PLX_OK. */
+ * its outputs are undefined), PLX_ERR_BOUNDS if a device-side index check of
+ * a debug build failed (below), PLX_ERR_CUDA if the stream reports an error,
+ * else PLX_OK.
+ *
+ * Debug build: the same sources compiled with PLX_DEBUG_BOUNDS
+ * (python -m parametrized_local_linear_gb300.build --debug-bounds, giving
+ * libplx_debug.so with this same interface) check, before each TMA copy and
+ * each indexed global store, that the coordinates or index lie inside the
+ * buffer: the tensor-map coordinates of every prefill, backward and
+ * projection box, every decode box against its sequence's tokens, and the
+ * decode's query rows and record slots. A failed check skips the access,
+ * stops the CTA as a timed-out wait does and sets the bit that this call
+ * reports as PLX_ERR_BOUNDS; nothing traps. Outputs of a call that passed
+ * every check equal the release library's bit for bit. */
 plx_status plx_check_device_error(void *stream);
 
 /* Launches one block whose wait on an mbarrier that nothing ever arrives on

@@ -23,6 +23,7 @@ PLX_ERR_INVALID_ARG = 1
 PLX_ERR_UNSUPPORTED = 2
 PLX_ERR_CUDA = 3
 PLX_ERR_DEVICE_TIMEOUT = 4
+PLX_ERR_BOUNDS = 5
 
 # Every symbol the header declares, with its ctypes signature.
 _vp, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
@@ -73,6 +74,18 @@ def lib():
                 f.argtypes = args
             _lib = L
     return _lib
+
+
+def load_debug_lib():
+    """libplx_debug.so, the build with device-side bounds checks (see
+    include/plx.h), loaded with the same signatures; built if missing."""
+    from . import build
+    L = ctypes.CDLL(build.build(debug_bounds=True))
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
 
 
 def _check(status: int):

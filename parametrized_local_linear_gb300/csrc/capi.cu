@@ -422,6 +422,11 @@ plx_status plx_check_device_error(void *stream) {
   if (e != cudaSuccess) return cuda_fail(e, "plx_check_device_error: read");
   if (v & plx::kErrTimeout)
     return fail(PLX_ERR_DEVICE_TIMEOUT, "a bounded in-kernel wait ran out (error word 0x%x)", v);
+  if (v & plx::kErrBounds)
+    return fail(PLX_ERR_BOUNDS,
+                "a device-side bounds check failed; the access was skipped and the outputs "
+                "are undefined (error word 0x%x)",
+                v);
   if (v & plx::kErrBadInput)
     return fail(PLX_ERR_INVALID_ARG,
                 "a kernel found device-side inputs out of range (decode: seqlens sum to 2^30 "
@@ -445,6 +450,7 @@ const char *plx_status_string(plx_status s) {
     case PLX_ERR_UNSUPPORTED: return "unsupported configuration";
     case PLX_ERR_CUDA: return "CUDA error";
     case PLX_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case PLX_ERR_BOUNDS: return "device bounds check failed";
     default: return "unknown status";
   }
 }

@@ -279,9 +279,18 @@ __global__ void __launch_bounds__(THREADS)
             ok = false;
             break;
           }
+          const int z = min(first + KT * t, last - KT);
+          // The box stays inside the item's tokens (or, for a cache shorter
+          // than one box, starts before token 0, where TMA zero-fills).
+          if (!PLX_IN_BOUNDS(it.b < a.B && it.kvh < a.Hkv && z + KT <= last &&
+                                 static_cast<long long>(last) * a.Hkv <= pl.W &&
+                                 (z >= 0 || last < KT),
+                             ab)) {
+            ok = false;
+            break;
+          }
           const uint32_t bar = smem_u32(&full[st]);
           mbar_arrive_expect_tx(bar, STAGE_BYTES);
-          const int z = min(first + KT * t, last - KT);
           const uint32_t base = smem_u32(smem + st * STAGE_BYTES);
           tma_load_3d(base, &tm_k, 0, it.kvh, z, bar);
           tma_load_3d(base + HALF, &tm_k, 64, it.kvh, z, bar);
@@ -314,8 +323,15 @@ __global__ void __launch_bounds__(THREADS)
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     uint32_t qa[8][4];
+    // The item's query rows and record slots lie inside q, r and the records.
+    const bool item_ok = PLX_IN_BOUNDS(
+        it.b < a.B && it.kvh < a.Hkv &&
+            static_cast<long long>(it.b) * a.Hq + static_cast<long long>(it.kvh + 1) * a.G <=
+                static_cast<long long>(a.B) * a.Hq &&
+            c + it.b * a.Hkv + it.kvh < pl.n + a.B * a.Hkv,
+        ab);
     {
-      const bool live = g < a.G;
+      const bool live = g < a.G && item_ok;
       const size_t hrow = (static_cast<size_t>(it.b) * a.Hq + it.kvh * a.G + (live ? g : 0)) * D;
       const uint32_t *qr = reinterpret_cast<const uint32_t *>(a.q + hrow);
       const uint32_t *rr = reinterpret_cast<const uint32_t *>(a.r + hrow);
@@ -429,6 +445,7 @@ __global__ void __launch_bounds__(THREADS)
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NCW; ++w) M = fmaxf(M, mls[(w * a.G + gh) * 3]);
+      if (!item_ok) continue;
       float *rec = a.recs + (static_cast<size_t>(c + row) * a.G + gh) * REC;
       if (M == -INFINITY || aborted) {
         rec[dim] = 0.f;
@@ -456,7 +473,7 @@ __global__ void __launch_bounds__(THREADS)
         rec[2 * D + 1] = M + log2f(L);
       }
     }
-    if (it.k0 == 0 && dim == 0) {
+    if (it.k0 == 0 && dim == 0 && item_ok) {
       // This CTA holds the row's first key, so it is the first of the CTAs
       // that hold the row (CTA c' writes its records to slot c' + row); the
       // last one holds the row's last key x, CTA floor(((x + 1) n - 1) / W).

@@ -21,6 +21,20 @@ constexpr unsigned kErrTimeout = 1u;
 // A kernel found its device-side inputs out of range (decode: the lengths sum
 // to 2^30 tokens or more) and did no work.
 constexpr unsigned kErrBadInput = 2u;
+// A debug bounds check failed: an index about to be used lay outside its
+// buffer, and the access was skipped (builds with PLX_DEBUG_BOUNDS only).
+constexpr unsigned kErrBounds = 4u;
+
+// PLX_IN_BOUNDS(cond, ab) is true when cond holds. Built with
+// PLX_DEBUG_BOUNDS, a false cond raises the CTA's abort flag and sets
+// kErrBounds in the device error word, and the caller skips the access and
+// drains as after a timed-out wait; nothing traps. Built without it, the
+// macro is the constant true and cond is not evaluated.
+#ifdef PLX_DEBUG_BOUNDS
+#define PLX_IN_BOUNDS(cond, ab) ((cond) ? true : ((ab).raise(::plx::kErrBounds), false))
+#else
+#define PLX_IN_BOUNDS(cond, ab) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -259,15 +259,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       // ---------------------------------------------------------- producer
       const uint32_t qb = smem_u32(q_full);
-      mbar_arrive_expect_tx(qb, 6 * HALF_Q);
+      const bool in_bounds = PLX_IN_BOUNDS(q0 >= 0 && q0 < a.L && zq < a.B * a.Hq && zk < a.B * a.Hkv &&
+                                               (n - 1) * BN < a.L,
+                                           ab);
+      if (in_bounds) mbar_arrive_expect_tx(qb, 6 * HALF_Q);
+      if (in_bounds) {
       tma_load_3d(smem_u32(smem + OFF_Q), &tm_q, 0, q0, zq, qb);
       tma_load_3d(smem_u32(smem + OFF_Q + HALF_Q), &tm_q, 64, q0, zq, qb);
       tma_load_3d(smem_u32(smem + OFF_R), &tm_r, 0, q0, zq, qb);
       tma_load_3d(smem_u32(smem + OFF_R + HALF_Q), &tm_r, 64, q0, zq, qb);
       tma_load_3d(smem_u32(smem + OFF_DO), &tm_do, 0, q0, zq, qb);
       tma_load_3d(smem_u32(smem + OFF_DO + HALF_Q), &tm_do, 64, q0, zq, qb);
+      }
       int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n; ++j) {
+      for (int j = 0; in_bounds && j < n; ++j) {
         const int st = j % NST;
         if (j >= NST && !mbar_wait(smem_u32(&k_empty[st]), ((j / NST) - 1) & 1, ab)) break;
         const uint32_t kf = smem_u32(&k_full[st]);
@@ -285,7 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         v_issued = j + 1;
       }
       if (ab.raised()) {
-        mbar_wait_drain(qb, 0);
+        if (in_bounds) mbar_wait_drain(qb, 0);
         for (int j = max(0, k_issued - NST); j < k_issued; ++j)
           mbar_wait_drain(smem_u32(&k_full[j % NST]), (j / NST) & 1);
         for (int j = max(0, v_issued - NST); j < v_issued; ++j)
@@ -512,16 +517,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       // ---------------------------------------------------------- producer
       const uint32_t kvb = smem_u32(kv_full);
-      mbar_arrive_expect_tx(kvb, 4 * HALF_K);
+      const bool in_bounds = PLX_IN_BOUNDS(k0 >= 0 && k0 < a.L && zk < a.B * a.Hkv &&
+                                               (b * a.Hq + (kvh + 1) * G) <= a.B * a.Hq,
+                                           ab);
+      if (in_bounds) mbar_arrive_expect_tx(kvb, 4 * HALF_K);
+      if (in_bounds) {
       tma_load_3d(smem_u32(smem + OFF_K), &tm_k, 0, k0, zk, kvb);
       tma_load_3d(smem_u32(smem + OFF_K + HALF_K), &tm_k, 64, k0, zk, kvb);
       tma_load_3d(smem_u32(smem + OFF_V), &tm_v, 0, k0, zk, kvb);
       tma_load_3d(smem_u32(smem + OFF_V + HALF_K), &tm_v, 64, k0, zk, kvb);
+      }
       int issued = 0;
-      for (int s = 0; s < n; ++s) {
+      for (int s = 0; in_bounds && s < n; ++s) {
         const int st = s % NST;
         if (s >= NST && !mbar_wait(smem_u32(&q_empty[st]), ((s / NST) - 1) & 1, ab)) break;
         const int zq = b * a.Hq + kvh * G + s / per_head, y = (qt_lo + s % per_head) * BN;
+        if (!PLX_IN_BOUNDS(zq < a.B * a.Hq && y < a.L, ab)) break;
         const uint32_t qf = smem_u32(&q_full[st]);
         const uint32_t base = smem_u32(smem + OFF_STG + st * STAGE);
         mbar_arrive_expect_tx(qf, STAGE);
@@ -534,7 +545,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         issued = s + 1;
       }
       if (ab.raised()) {
-        mbar_wait_drain(kvb, 0);
+        if (in_bounds) mbar_wait_drain(kvb, 0);
         for (int s = max(0, issued - NST); s < issued; ++s)
           mbar_wait_drain(smem_u32(&q_full[s % NST]), (s / NST) & 1);
       }

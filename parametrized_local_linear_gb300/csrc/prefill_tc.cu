@@ -195,6 +195,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int k = 0; ok && item_of(a, k, it); ++k) {
         // Q and R of the previous item are dead once its last S/T UMMAs finish.
         if (k > 0 && !mbar_wait(smem_u32(q_empty), (k - 1) & 1, ab)) break;
+        // Every box of the item lies inside its head's rows (TMA zero-fills
+        // past L or Lk only within a head).
+        if (!PLX_IN_BOUNDS(it.q0 >= 0 && it.q0 < a.L && it.zq >= 0 && it.zq < a.B * a.Hq &&
+                               it.zk >= 0 && it.zk < a.B * a.Hkv && it.ntiles >= 1 &&
+                               (it.ntiles - 1) * BN < a.Lk,
+                           ab))
+          break;
         mbar_arrive_expect_tx(qb, 4 * HALF_Q);
         tma_load_3d(smem_u32(smem + OFF_Q), &tm_q, 0, it.q0, it.zq, qb);
         tma_load_3d(smem_u32(smem + OFF_Q + HALF_Q), &tm_q, 64, it.q0, it.zq, qb);
@@ -442,6 +449,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Correction (Sigma rho) = O2/l - (O1/l)(sigma/l); o = O1/l - correction.
       const float gc = sg * inv * inv;
       const bool want_cor = a.cor != nullptr;
+      const bool row_ok = grow < a.L &&
+                          PLX_IN_BOUNDS(it.zq >= 0 && it.zq < a.B * a.Hq && grow >= 0, ab);
       float csq = 0.f, osq = 0.f;
       __nv_bfloat16 *orow = a.out + (static_cast<size_t>(it.zq) * a.L + grow) * D;
 #pragma unroll 1
@@ -466,7 +475,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             osq = fmaf(x0, x0, fmaf(x1, x1, osq));
           }
         }
-        if (grow < a.L) {
+        if (row_ok) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + part * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
@@ -480,10 +489,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if (a.lse != nullptr && grow < a.L)
+      if (a.lse != nullptr && row_ok)
         a.lse[static_cast<size_t>(it.zq) * a.L + grow] = (m_used + log2f(l)) * 0.6931471805599453f;
-      if (a.sbar != nullptr && grow < a.L) a.sbar[static_cast<size_t>(it.zq) * a.L + grow] = sg * inv;
-      if (want_cor && grow < a.L)
+      if (a.sbar != nullptr && row_ok) a.sbar[static_cast<size_t>(it.zq) * a.L + grow] = sg * inv;
+      if (want_cor && row_ok)
         a.cor[static_cast<size_t>(it.zq) * a.L + grow] = osq > 0.f ? sqrtf(csq) / sqrtf(osq) : 0.f;
     }
   }

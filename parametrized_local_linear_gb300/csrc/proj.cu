@@ -50,6 +50,7 @@ struct ProjArgs {
   __nv_bfloat16 *q, *k, *v, *r;
   int T, L, Hq, Hkv;     // tokens (B L), tokens per sequence, heads
   int mtp, npairs, kt;   // token-tile pairs, tile pairs (clusters' work units), K stages
+  int D, F;              // model dim, stacked output features (2 Hq + 2 Hkv) d
   unsigned *err;
 };
 
@@ -110,6 +111,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int kk = 0; kk < a.kt; ++kk, ++g) {
           const int st = g % NST;
           if (g >= NST && !mbar_wait(smem_u32(&empty[st]), ((g / NST) - 1) & 1, ab)) { ok = false; break; }
+          // The W box lies inside W's rows and both boxes inside the model dim
+          // (x rows past the tokens are zero-filled by TMA).
+          if (!PLX_IN_BOUNDS(kk * BK < a.D && n0 + crank * (BN / 2) < a.F, ab)) { ok = false; break; }
           // The leader's barrier counts both CTAs' 32 KB.
           if (leader) mbar_arrive_expect_tx(smem_u32(&full[st]), 2 * STAGE);
           const uint32_t fb = mapa_shared(smem_u32(&full[st]), 0);
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         else if (f < fk) { dst = a.k; H = a.Hkv; fo = f - fq; }
         else if (f < fv) { dst = a.v; H = a.Hkv; fo = f - fk; }
         else { dst = a.r; H = a.Hq; fo = f - fv; }
-        if (valid) {
+        if (valid && PLX_IN_BOUNDS(fo / HD < H && fo % HD + 32 <= HD && f < a.F, ab)) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(vals[e], vals[e + 1]);
@@ -259,6 +263,8 @@ cudaError_t launch_qkvr_proj(const void *x, const void *w, void *q, void *k, voi
   a.mtp = (mt + 1) / 2;  // an odd last tile's partner reads zero rows and stores nothing
   a.npairs = a.mtp * (F / BN);  // F = 256 (Hq + Hkv): whole feature tiles
   a.kt = (D + BK - 1) / BK;
+  a.D = D;
+  a.F = F;
   a.err = err;
   const int clusters = min(a.npairs, sm_count() / 2);
   cudaLaunchConfig_t cfg = {};

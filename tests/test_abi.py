@@ -141,3 +141,12 @@ def test_noalloc_decode_rejects_bad_arguments_before_any_cuda_call(lib):
     assert f(p, p, p, p, p, p, 2, 4, 2, 64, None) == binding.PLX_ERR_UNSUPPORTED
     assert f(p, p, p, p, p, ctypes.c_void_p(4100), 2, 4, 2, 128, None) == binding.PLX_ERR_INVALID_ARG
     assert b"aligned" in lib.plx_last_error_message()
+
+
+def test_debug_bounds_build_exports_every_symbol():
+    """The PLX_DEBUG_BOUNDS build compiles for sm_103a and has the same
+    interface (a CPU check; its GPU run is in test_debug_bounds_gpu.py)."""
+    dbg = binding.load_debug_lib()
+    for s in declared_symbols():
+        assert hasattr(dbg, s), s
+    assert dbg.plx_status_string(binding.PLX_ERR_BOUNDS) == b"device bounds check failed"
