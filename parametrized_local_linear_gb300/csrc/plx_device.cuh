@@ -110,6 +110,38 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
   }
 }
 
+// Non-blocking probe of phase `parity` of `bar`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for the single issuing threads on a kernel's critical path: it
+// polls instead of suspending, so the thread proceeds as soon as the phase
+// completes rather than when the hardware wakes it. Same bound and abort
+// behaviour as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, const Abort &ab,
+                                               long long limit = kSpinLimitCycles) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (ab.raised()) return false;
+    if (clock64() - t0 > limit) {
+      ab.raise(kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // Wait that ignores the abort flag (used to drain a thread's own in-flight
 // asynchronous copies before exiting); still bounded.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {

@@ -135,11 +135,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *v_full = k_empty + NST;
   uint64_t *v_empty = v_full + NST;    // count 2 (O1 and O2)
   uint64_t *st_full = v_empty + NST;   // [2] count 2
-  uint64_t *p_full = st_full + 2;      // [2][2] count 128: P of keys [32 h, 32 h + 32) of buffer x
+  uint64_t *p_full = st_full + 2;      // [2][2] count 4 (a lane per softmax warp): P of keys [32 h, 32 h + 32) of buffer x
   uint64_t *pv_done = p_full + 4;      // [2] count 2: value UMMAs of the tiles in buffer x
   uint64_t *pv_issued = pv_done + 2;   // [2][2]: O1 (h = 0) / O2 (h = 1) value UMMAs of buffer x issued
-  uint64_t *o_free = pv_issued + 4;      // count 128: the epilogue has read O1 and O2
-  uint64_t *stat_full = o_free + 1;    // [2] count 128: row statistics of an item written
+  uint64_t *o_free = pv_issued + 4;      // count 4 (a lane per epilogue warp): the epilogue has read O1 and O2
+  uint64_t *stat_full = o_free + 1;    // [2] count 4: row statistics of an item written
   uint64_t *drain = stat_full + 2;     // [4]: one per issuing thread
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -157,14 +157,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(smem_u32(&st_full[x]), 2);
-      mbar_init(smem_u32(&p_full[2 * x]), 128);
-      mbar_init(smem_u32(&p_full[2 * x + 1]), 128);
+      mbar_init(smem_u32(&p_full[2 * x]), 4);
+      mbar_init(smem_u32(&p_full[2 * x + 1]), 4);
       mbar_init(smem_u32(&pv_done[x]), 2);
       mbar_init(smem_u32(&pv_issued[2 * x]), 1);
       mbar_init(smem_u32(&pv_issued[2 * x + 1]), 1);
-      mbar_init(smem_u32(&stat_full[x]), 128);
+      mbar_init(smem_u32(&stat_full[x]), 4);
     }
-    mbar_init(smem_u32(o_free), 128);
+    mbar_init(smem_u32(o_free), 4);
     for (int x = 0; x < 4; ++x) mbar_init(smem_u32(&drain[x]), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int k = 0; ok && item_of(a, k, it); ++k) {
         for (int j = 0; j < it.ntiles; ++j) {
           const int gg = g + j, x = gg & 1, st = gg % NST;
-          if (!mbar_wait(smem_u32(&p_full[2 * x]), (gg >> 1) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait_spin(smem_u32(&p_full[2 * x]), (gg >> 1) & 1, ab)) { ok = false; break; }
           // The first value UMMA of an item overwrites O: the previous item's
           // epilogue must have read it.
           if (j == 0 && k > 0 && !mbar_wait(smem_u32(o_free), (k - 1) & 1, ab)) { ok = false; break; }
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t ap = tbase + (x ? COL_S1 : COL_S0) + col_off;
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks) {
-            if (ks == 2 && !mbar_wait(smem_u32(&p_full[2 * x + 1]), (gg >> 1) & 1, ab)) { ok = false; break; }
+            if (ks == 2 && !mbar_wait_spin(smem_u32(&p_full[2 * x + 1]), (gg >> 1) & 1, ab)) { ok = false; break; }
             umma_ts(dout, ap + ks * 8, vdesc + ks * (2048 >> 4), idesc_pv, (j > 0 || ks > 0));
           }
           if (!ok) break;
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int gg = g + j, x = gg & 1, st = gg % NST;
           // Buffer x holds P (P o T) of CTA tile gg - 2: its value UMMAs must
           // have been issued; issued earlier, they execute first.
-          if (gg >= 2 && !mbar_wait(smem_u32(&pv_issued[2 * x + (is_s ? 0 : 1)]), ((gg - 2) >> 1) & 1, ab)) { ok = false; break; }
+          if (gg >= 2 && !mbar_wait_spin(smem_u32(&pv_issued[2 * x + (is_s ? 0 : 1)]), ((gg - 2) >> 1) & 1, ab)) { ok = false; break; }
           if (!mbar_wait(smem_u32(&k_full[st]), (gg / NST) & 1, ab)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kdesc = kdesc0 + st * (TILE_KV >> 4);
@@ -409,7 +409,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // P of keys [0, 32) is in place: its value UMMAs may start.
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&p_full[2 * x]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&p_full[2 * x]));
           }
         }
         const uint64_t lsum = fadd2(lp[0], lp[1]), ssum = fadd2(sp[0], sp[1]);
@@ -417,7 +418,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         sg += f2lo(ssum) + f2hi(ssum);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&p_full[2 * x + 1]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_full[2 * x + 1]));
       }
       if (!ok) break;
       // Hand the row statistics to the epilogue and move on to the next item.
@@ -425,7 +427,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       st[row] = m_used;
       st[BM + row] = l;
       st[2 * BM + row] = sg;
-      mbar_arrive(smem_u32(&stat_full[k & 1]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&stat_full[k & 1]));
       g += n;
     }
   } else if (warp >= EP_WARP0 && warp < EP_WARP0 + 4) {
@@ -462,7 +465,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (part == 3) {
           // O has been read: the next item's value UMMAs may overwrite it.
           tc_fence_before();
-          mbar_arrive(smem_u32(o_free));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(o_free));
         }
         uint32_t pk[16];
 #pragma unroll
