@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *v_empty = k_empty + NST;    // U UMMAs of the tile done
   uint64_t *v_full = v_empty + NST;
   uint64_t *stu_full = v_full + NST;    // count 3: S, T, U of the tile in TMEM
-  uint64_t *stu_free = stu_full + 1;    // count 256: S, T, U loaded by every thread
-  uint64_t *gs_full = stu_free + 1;     // count 256: dS, dT written
+  uint64_t *stu_free = stu_full + 1;    // count 8 (a lane per elementwise warp): S, T, U loaded
+  uint64_t *gs_full = stu_free + 1;     // count 8: dS, dT written
   uint64_t *acc_done = gs_full + 1;     // count 2: dQ and dR UMMAs of the tile done
   uint64_t *acc_full = acc_done + 1;    // count 2: every gradient UMMA done (epilogue)
   uint64_t *drain = acc_full + 1;       // [3] one per issuing thread
@@ -230,8 +230,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
     mbar_init(smem_u32(stu_full), 3);
-    mbar_init(smem_u32(stu_free), NEW);
-    mbar_init(smem_u32(gs_full), NEW);
+    mbar_init(smem_u32(stu_free), NEW / 32);  // a lane per elementwise warp
+    mbar_init(smem_u32(gs_full), NEW / 32);
     mbar_init(smem_u32(acc_done), 2);
     mbar_init(smem_u32(acc_full), 2);
     for (int x = 0; x < 3; ++x) mbar_init(smem_u32(&drain[x]), 1);
@@ -332,10 +332,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n) {
           // S, T, U of tile j are in registers once stu_free completes.
-          if (!mbar_wait(smem_u32(stu_free), j & 1, ab) || !issue_score(j + 1)) break;
+          if (!mbar_wait_spin(smem_u32(stu_free), j & 1, ab) || !issue_score(j + 1)) break;
         }
         if (role == 2) continue;
-        if (!mbar_wait(smem_u32(gs_full), j & 1, ab)) break;
+        if (!mbar_wait_spin(smem_u32(gs_full), j & 1, ab)) break;
         tc_fence_after();
         const int st = j % NST;
         const uint64_t km = kmn0 + st * (TILE_KV >> 4);
@@ -375,7 +375,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld32(tl + COL_U + 32 * hf, u);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(smem_u32(stu_free));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(stu_free));
       const int kbase = j * BN + 32 * hf;
       uint32_t gs[16], gt[16];
       if (j * BN + BN - 1 > q0) {  // the tile reaches the diagonal
@@ -406,7 +407,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_st16(tl + COL_GT + 16 * hf, gt);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(gs_full));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(gs_full));
     }
     if (ok) {
       ok = mbar_wait(smem_u32(acc_full), 0, ab);
@@ -462,8 +464,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *q_full = bars + 1;          // [NST] Q, R, dO of a step loaded
   uint64_t *q_empty = q_full + NST;     // [NST] count 2: the step's dV and dK UMMAs done
   uint64_t *stu_full = q_empty + NST;   // count 3
-  uint64_t *stu_free = stu_full + 1;    // count 256
-  uint64_t *gs_full = stu_free + 1;     // count 256: (w c)^T in smem, dS^T / dT^T in TMEM
+  uint64_t *stu_free = stu_full + 1;    // count 8 (a lane per elementwise warp)
+  uint64_t *gs_full = stu_free + 1;     // count 8: (w c)^T in smem, dS^T / dT^T in TMEM
   uint64_t *acc_done = gs_full + 1;     // count 2
   uint64_t *acc_full = acc_done + 1;    // count 2
   uint64_t *drain = acc_full + 1;       // [3]
@@ -488,8 +490,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&q_empty[s]), 2);
     }
     mbar_init(smem_u32(stu_full), 2);  // [S^T | T^T] and U^T
-    mbar_init(smem_u32(stu_free), NEW);
-    mbar_init(smem_u32(gs_full), NEW);
+    mbar_init(smem_u32(stu_free), NEW / 32);  // a lane per elementwise warp
+    mbar_init(smem_u32(gs_full), NEW / 32);
     mbar_init(smem_u32(acc_done), 2);
     mbar_init(smem_u32(acc_full), 2);
     for (int x = 0; x < 3; ++x) mbar_init(smem_u32(&drain[x]), 1);
@@ -590,10 +592,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (scores) ok = ok && issue_score(0);
       for (int s = 0; ok && s < n; ++s) {
         if (scores && s + 1 < n) {
-          if (!mbar_wait(smem_u32(stu_free), s & 1, ab) || !issue_score(s + 1)) break;
+          if (!mbar_wait_spin(smem_u32(stu_free), s & 1, ab) || !issue_score(s + 1)) break;
         }
         if (role == 2) continue;
-        if (!mbar_wait(smem_u32(gs_full), s & 1, ab)) break;
+        if (!mbar_wait_spin(smem_u32(gs_full), s & 1, ab)) break;
         const int st = s % NST;
         // The stage's loads completed before its score products ran (role 0
         // waited on q_full); role 1 observes that too before reading Q and R.
@@ -648,7 +650,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_ld32(tl + COL_U + 32 * hf, uv);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(smem_u32(stu_free));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(stu_free));
       uint32_t gs[16], gt[16], pc[16];
       auto cols = [&](auto mask_tag) {
         constexpr bool M = decltype(mask_tag)::value;
@@ -686,7 +689,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_u32(gs_full));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(gs_full));
     }
     if (ok) {
       ok = mbar_wait(smem_u32(acc_full), 0, ab);
