@@ -251,11 +251,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int k = 0; ok && item_of(a, k, it); ++k) {
         for (int j = 0; j < it.ntiles; ++j) {
           const int gg = g + j, x = gg & 1, st = gg % NST;
-          if (!mbar_wait_spin(smem_u32(&p_full[2 * x]), (gg >> 1) & 1, ab)) { ok = false; break; }
+          // V and O are normally ready long before P: waiting on them first
+          // leaves only the P hand-over between the softmax and the issue.
           // The first value UMMA of an item overwrites O: the previous item's
           // epilogue must have read it.
           if (j == 0 && k > 0 && !mbar_wait(smem_u32(o_free), (k - 1) & 1, ab)) { ok = false; break; }
           if (!mbar_wait(smem_u32(&v_full[st]), (gg / NST) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait_spin(smem_u32(&p_full[2 * x]), (gg >> 1) & 1, ab)) { ok = false; break; }
           tc_fence_after();
           const uint64_t vdesc = vdesc0 + st * (TILE_KV >> 4);
           const uint32_t ap = tbase + (x ? COL_S1 : COL_S0) + col_off;
@@ -295,10 +297,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(smem_u32(q_full), k & 1, ab)) break;
         for (int j = 0; j < it.ntiles; ++j) {
           const int gg = g + j, x = gg & 1, st = gg % NST;
-          // Buffer x holds P (P o T) of CTA tile gg - 2: its value UMMAs must
-          // have been issued; issued earlier, they execute first.
-          if (gg >= 2 && !mbar_wait_spin(smem_u32(&pv_issued[2 * x + (is_s ? 0 : 1)]), ((gg - 2) >> 1) & 1, ab)) { ok = false; break; }
+          // K is normally loaded well ahead: wait for it first. Buffer x holds
+          // P (P o T) of CTA tile gg - 2: its value UMMAs must have been
+          // issued; issued earlier, they execute first.
           if (!mbar_wait(smem_u32(&k_full[st]), (gg / NST) & 1, ab)) { ok = false; break; }
+          if (gg >= 2 && !mbar_wait_spin(smem_u32(&pv_issued[2 * x + (is_s ? 0 : 1)]), ((gg - 2) >> 1) & 1, ab)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kdesc = kdesc0 + st * (TILE_KV >> 4);
           const uint32_t d = tbase + (x ? COL_S1 : COL_S0) + col_off;
