@@ -315,9 +315,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t acol = tbase + (role == 0 ? COL_ACC0 : COL_ACC1);
       uint64_t *b_full = role == 2 ? v_full : k_full;
       bool ok = mbar_wait(smem_u32(q_full), 0, ab);
+      // The operand stage of tile j is normally loaded before S, T, U of tile
+      // j - 1 are free: wait for it first, so that only that hand-over
+      // stands before the issue.
+      auto operand_ready = [&](int j) -> bool {
+        return mbar_wait(smem_u32(&b_full[j % NST]), (j / NST) & 1, ab);
+      };
       auto issue_score = [&](int j) -> bool {
         const int st = j % NST;
-        if (!mbar_wait(smem_u32(&b_full[st]), (j / NST) & 1, ab)) return false;
         tc_fence_after();
         const uint64_t bd = bdesc0 + st * (TILE_KV >> 4);
 #pragma unroll
@@ -328,11 +333,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (role == 2) umma_commit(smem_u32(&v_empty[st]));
         return true;
       };
-      ok = ok && issue_score(0);
+      ok = ok && operand_ready(0) && issue_score(0);
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n) {
           // S, T, U of tile j are in registers once stu_free completes.
-          if (!mbar_wait_spin(smem_u32(stu_free), j & 1, ab) || !issue_score(j + 1)) break;
+          if (!operand_ready(j + 1) || !mbar_wait_spin(smem_u32(stu_free), j & 1, ab) ||
+              !issue_score(j + 1))
+            break;
         }
         if (role == 2) continue;
         if (!mbar_wait_spin(smem_u32(gs_full), j & 1, ab)) break;
@@ -577,9 +584,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t dcol = tbase + (role == 2 ? COL_U : COL_S);
       const uint32_t idesc_s = role == 2 ? idesc_u : idesc_st;
       bool ok = mbar_wait(smem_u32(kv_full), 0, ab);
+      auto operand_ready = [&](int s) -> bool {
+        return mbar_wait(smem_u32(&q_full[s % NST]), (s / NST) & 1, ab);
+      };
       auto issue_score = [&](int s) -> bool {
         const int st = s % NST;
-        if (!mbar_wait(smem_u32(&q_full[st]), (s / NST) & 1, ab)) return false;
         tc_fence_after();
         const uint64_t bd = stg_k + st * (STAGE >> 4);
 #pragma unroll
@@ -589,10 +598,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         umma_commit(smem_u32(stu_full));
         return true;
       };
-      if (scores) ok = ok && issue_score(0);
+      if (scores) ok = ok && operand_ready(0) && issue_score(0);
       for (int s = 0; ok && s < n; ++s) {
         if (scores && s + 1 < n) {
-          if (!mbar_wait_spin(smem_u32(stu_free), s & 1, ab) || !issue_score(s + 1)) break;
+          if (!operand_ready(s + 1) || !mbar_wait_spin(smem_u32(stu_free), s & 1, ab) ||
+              !issue_score(s + 1))
+            break;
         }
         if (role == 2) continue;
         if (!mbar_wait_spin(smem_u32(gs_full), s & 1, ab)) break;
