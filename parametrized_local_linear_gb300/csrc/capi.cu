@@ -422,6 +422,11 @@ plx_status plx_check_device_error(void *stream) {
   if (e != cudaSuccess) return cuda_fail(e, "plx_check_device_error: read");
   if (v & plx::kErrTimeout)
     return fail(PLX_ERR_DEVICE_TIMEOUT, "a bounded in-kernel wait ran out (error word 0x%x)", v);
+  if (v & plx::kErrLayout)
+    return fail(PLX_ERR_CUDA,
+                "a kernel's dynamic shared memory was not 1024-byte aligned; it did no work "
+                "(error word 0x%x)",
+                v);
   if (v & plx::kErrBounds)
     return fail(PLX_ERR_BOUNDS,
                 "a device-side bounds check failed; the access was skipped and the outputs "

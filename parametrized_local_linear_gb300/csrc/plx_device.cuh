@@ -24,6 +24,9 @@ constexpr unsigned kErrBadInput = 2u;
 // A debug bounds check failed: an index about to be used lay outside its
 // buffer, and the access was skipped (builds with PLX_DEBUG_BOUNDS only).
 constexpr unsigned kErrBounds = 4u;
+// A kernel found its dynamic shared memory not 1024-byte aligned, which its
+// 128-byte-swizzled tiles need, and did no work (not expected to happen).
+constexpr unsigned kErrLayout = 8u;
 
 // PLX_IN_BOUNDS(cond, ab) is true when cond holds. Built with
 // PLX_DEBUG_BOUNDS, a false cond raises the CTA's abort flag and sets
@@ -153,6 +156,17 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------- TMA
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`; both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // 3-D tiled tensor load (box and swizzle come from the tensor map).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
                                             uint32_t bar) {

@@ -453,9 +453,17 @@ constexpr int STAGE = 3 * TILE_Q;
 constexpr int OFF_K = 0, OFF_V = 2 * HALF_K;
 constexpr int OFF_P = 4 * HALF_K;              // 65536: (w c)^T tile, 128 keys x 64 queries bf16
 constexpr int OFF_STG = OFF_P + BM * BN * 2;   // 81920
-constexpr int OFF_BAR = OFF_STG + NST * STAGE; // 229376
-constexpr int NBAR = 1 + 2 * NST + 5 + 3;
-constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
+// The per-row records of a step's 64 queries (1 KB, 32 row pairs of 32 bytes)
+// in a ring of their own, read by every elementwise lane as broadcasts.
+constexpr int REC_STAGES = 2;
+constexpr int REC_BYTES = BN * 16;
+constexpr int OFF_REC = OFF_STG + NST * STAGE;  // 229376
+constexpr int OFF_BAR = OFF_REC + REC_STAGES * REC_BYTES;
+constexpr int NBAR = 1 + 2 * NST + 5 + 3 + 2 * REC_STAGES;
+// No alignment slack: the dynamic shared memory starts 1024-byte aligned
+// (checked at run time), which is what leaves room for the records.
+constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
+static_assert(SMEM_BYTES <= 232448, "dK/dV kernel shared memory");
 }  // namespace kv
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -463,9 +471,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
   using namespace kv;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw;
+  if ((smem_u32(smem_raw) & 1023u) != 0u) {
+    // The swizzled tiles need a 1024-byte aligned base; never expected.
+    if (threadIdx.x == 0 && a.err) atomicOr(a.err, kErrLayout);
+    return;
+  }
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *kv_full = bars;             // K and V blocks loaded
   uint64_t *q_full = bars + 1;          // [NST] Q, R, dO of a step loaded
@@ -476,6 +488,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *acc_done = gs_full + 1;     // count 2
   uint64_t *acc_full = acc_done + 1;    // count 2
   uint64_t *drain = acc_full + 1;       // [3]
+  uint64_t *rec_full = drain + 3;       // [REC_STAGES] a step's records loaded
+  uint64_t *rec_empty = rec_full + REC_STAGES;  // [REC_STAGES] count 8: read by every elementwise warp
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -502,6 +516,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(smem_u32(acc_done), 2);
     mbar_init(smem_u32(acc_full), 2);
     for (int x = 0; x < 3; ++x) mbar_init(smem_u32(&drain[x]), 1);
+    for (int x = 0; x < REC_STAGES; ++x) {
+      mbar_init(smem_u32(&rec_full[x]), 1);
+      mbar_init(smem_u32(&rec_empty[x]), NEW / 32);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -526,6 +544,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       // ---------------------------------------------------------- producer
       const uint32_t kvb = smem_u32(kv_full);
+      int rec_issued = 0;
       const bool in_bounds = PLX_IN_BOUNDS(k0 >= 0 && k0 < a.L && zk < a.B * a.Hkv &&
                                                (b * a.Hq + (kvh + 1) * G) <= a.B * a.Hq,
                                            ab);
@@ -552,11 +571,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_3d(base + 2 * TILE_Q, &tm_do, 0, y, zq, qf);
         tma_load_3d(base + 2 * TILE_Q + HALF_Q, &tm_do, 64, y, zq, qf);
         issued = s + 1;
+        // The step's 64 query records, contiguous in the record array.
+        const int rs = s % REC_STAGES;
+        if (s >= REC_STAGES && !mbar_wait(smem_u32(&rec_empty[rs]), ((s / REC_STAGES) - 1) & 1, ab)) break;
+        if (!PLX_IN_BOUNDS(y + BN <= a.Lpad, ab)) break;
+        const uint32_t rf = smem_u32(&rec_full[rs]);
+        mbar_arrive_expect_tx(rf, REC_BYTES);
+        bulk_g2s(smem_u32(smem + OFF_REC + rs * REC_BYTES),
+                 a.stats + (static_cast<size_t>(zq) * a.Lpad + y) * 4, REC_BYTES, rf);
+        rec_issued = s + 1;
       }
       if (ab.raised()) {
         if (in_bounds) mbar_wait_drain(kvb, 0);
         for (int s = max(0, issued - NST); s < issued; ++s)
           mbar_wait_drain(smem_u32(&q_full[s % NST]), (s / NST) & 1);
+        for (int s = max(0, rec_issued - REC_STAGES); s < rec_issued; ++s)
+          mbar_wait_drain(smem_u32(&rec_full[s % REC_STAGES]), (s / REC_STAGES) & 1);
       }
     }
   } else if (warp < EW_WARP0) {
@@ -644,15 +674,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint64_t c2 = f2(a.scale_log2, a.scale_log2), tau2 = f2(a.tau, a.tau);
     bool ok = true;
     for (int s = 0; s < n; ++s) {
-      const int zq = b * a.Hq + kvh * G + s / per_head;
       const int qbase = (qt_lo + s % per_head) * BN + 32 * hf;
-      // The records of this half's 32 queries are 16 pairs x 32 bytes: lane l
-      // loads 16 of them (pair l / 2, half l & 1), before the TMEM wait so the
-      // load overlaps it, and the pairs are handed round by warp shuffles
-      // (per-column loads from every lane stalled on their latency).
-      const float4 mine = __ldg(reinterpret_cast<const float4 *>(
-                                    a.stats + (static_cast<size_t>(zq) * a.Lpad + qbase) * 4) + lane);
-      ok = mbar_wait(smem_u32(stu_full), s & 1, ab);
+      // The records of this half's 32 queries: 16 row pairs of two float4,
+      // {-lse log2 e, 1 + sbar} and {a, -D} of both rows, read from the
+      // step's record stage as broadcasts (every lane the same address).
+      const int rs = s % REC_STAGES;
+      const float4 *rec4 =
+          reinterpret_cast<const float4 *>(smem + OFF_REC + rs * REC_BYTES) + 32 * hf;
+      ok = mbar_wait(smem_u32(&rec_full[rs]), (s / REC_STAGES) & 1, ab);
+      ok = ok && mbar_wait(smem_u32(stu_full), s & 1, ab);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       float sv[32], tv[32], uv[32];
@@ -668,11 +698,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         constexpr bool M = decltype(mask_tag)::value;
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          // Pair (qbase + e, qbase + e + 1): lanes e and e + 1 hold it.
-          const Stat2 st2{f2(__shfl_sync(0xffffffffu, mine.x, e), __shfl_sync(0xffffffffu, mine.y, e)),
-                          f2(__shfl_sync(0xffffffffu, mine.z, e), __shfl_sync(0xffffffffu, mine.w, e)),
-                          f2(__shfl_sync(0xffffffffu, mine.x, e + 1), __shfl_sync(0xffffffffu, mine.y, e + 1)),
-                          f2(__shfl_sync(0xffffffffu, mine.z, e + 1), __shfl_sync(0xffffffffu, mine.w, e + 1))};
+          // Pair (qbase + e, qbase + e + 1): float4s e and e + 1 of the half.
+          const float4 r0 = rec4[e], r1 = rec4[e + 1];
+          const Stat2 st2{f2(r0.x, r0.y), f2(r0.z, r0.w), f2(r1.x, r1.y), f2(r1.z, r1.w)};
           const Grad2 g2 = grad_pair<M, true>(f2(sv[e], sv[e + 1]), f2(tv[e], tv[e + 1]),
                                               f2(uv[e], uv[e + 1]), st2, krow > qbase + e,
                                               krow > qbase + e + 1, c2, tau2);
@@ -684,6 +712,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // Mask only where the block reaches the causal diagonal.
       if (k0 + BM - 1 > (qt_lo + s % per_head) * BN) cols(std::true_type{});
       else cols(std::false_type{});
+      // The records are read: their stage may be reloaded.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rec_empty[rs]));
       if (s > 0) {
         ok = mbar_wait(smem_u32(acc_done), (s - 1) & 1, ab);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
