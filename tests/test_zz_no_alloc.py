@@ -28,6 +28,27 @@ def _call_noalloc(q, r, kc, vc, sl, out):
     assert st == binding.PLX_OK, binding.lib().plx_last_error_message()
 
 
+@pytest.mark.parametrize("lens,Hq,Hkv", [
+    ([1, 5, 33, 0, 200, 64], 4, 2),      # an empty sequence, a one-token one, sub-tile lengths
+    ([300, 301], 8, 1),                  # 8 query heads a kv head
+    ([3000, 17, 12000], 16, 8),          # rows cut between several CTAs
+])
+def test_noalloc_decode_matches_the_oracle(lens, Hq, Hkv):
+    """The allocation-free decode against the fp64 oracle directly, not only
+    against the allocating entry point."""
+    import oracle
+    from helpers import assert_bf16_close
+    dev = device()
+    q, r, kc, vc, sl = inputs.decode_inputs(len(lens), Hq, Hkv, 128, lens, torch.bfloat16, 0.05,
+                                            5 + len(lens))
+    qd, rd, kd, vd, sd = (t.to(dev) for t in (q, r, kc, vc, sl))
+    out = torch.full_like(qd, float("nan"))
+    _call_noalloc(qd, rd, kd, vd, sd, out)
+    plx_check_device_error()
+    ref, _ = oracle.decode(q, r, kc, vc, sl)
+    assert_bf16_close(out.double().cpu().numpy(), ref, f"no-alloc decode {lens}")
+
+
 def test_noalloc_decode_matches_allocating_decode_twice():
     dev = device()
     cases = [([700, 0, 33, 4100], 16, 8, 21), ([9000, 130], 4, 2, 22)]
