@@ -185,11 +185,18 @@ constexpr int OFF_Q = 0, OFF_R = 2 * HALF_Q, OFF_DO = 4 * HALF_Q;
 constexpr int OFF_K = 6 * HALF_Q;              // 98304
 constexpr int OFF_V = OFF_K + NST * TILE_KV;   // 147456
 constexpr int OFF_BAR = OFF_V + NST * TILE_KV; // 196608
-constexpr int NBAR = 1 + 4 * NST + 5 + 3;
+constexpr int NBAR = 1 + 4 * NST + 5 + 4;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;
+// 13 warps: 0 TMA producer; 1, 2, 3 issue S, T, U; 4 issues the gradient
+// products dQ and dR; 5..12 elementwise. The gradient products get a thread
+// of their own: a thread that issues the next tile's score products blocks
+// while the tensor queue is full and would take up the gradient hand-over
+// late.
+constexpr int Q_THREADS = 32 * 13;
+constexpr int Q_EW_WARP0 = 5;
 }  // namespace qk
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(qk::Q_THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
                   const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
@@ -200,15 +207,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *q_full = bars;              // Q, R, dO loaded
   uint64_t *k_full = bars + 1;
-  uint64_t *k_empty = k_full + NST;     // count 2: dQ and dR UMMAs of the tile done
+  uint64_t *k_empty = k_full + NST;     // dQ and dR UMMAs of the tile done
   uint64_t *v_empty = k_empty + NST;    // U UMMAs of the tile done
   uint64_t *v_full = v_empty + NST;
   uint64_t *stu_full = v_full + NST;    // count 3: S, T, U of the tile in TMEM
   uint64_t *stu_free = stu_full + 1;    // count 8 (a lane per elementwise warp): S, T, U loaded
   uint64_t *gs_full = stu_free + 1;     // count 8: dS, dT written
-  uint64_t *acc_done = gs_full + 1;     // count 2: dQ and dR UMMAs of the tile done
-  uint64_t *acc_full = acc_done + 1;    // count 2: every gradient UMMA done (epilogue)
-  uint64_t *drain = acc_full + 1;       // [3] one per issuing thread
+  uint64_t *acc_done = gs_full + 1;     // dQ and dR UMMAs of the tile done
+  uint64_t *acc_full = acc_done + 1;    // every gradient UMMA done (epilogue)
+  uint64_t *drain = acc_full + 1;       // [4] one per issuing thread
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBAR);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -225,16 +232,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(smem_u32(q_full), 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
-      mbar_init(smem_u32(&k_empty[s]), 2);
+      mbar_init(smem_u32(&k_empty[s]), 1);
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
     mbar_init(smem_u32(stu_full), 3);
     mbar_init(smem_u32(stu_free), NEW / 32);  // a lane per elementwise warp
     mbar_init(smem_u32(gs_full), NEW / 32);
-    mbar_init(smem_u32(acc_done), 2);
-    mbar_init(smem_u32(acc_full), 2);
-    for (int x = 0; x < 3; ++x) mbar_init(smem_u32(&drain[x]), 1);
+    mbar_init(smem_u32(acc_done), 1);
+    mbar_init(smem_u32(acc_full), 1);
+    for (int x = 0; x < 4; ++x) mbar_init(smem_u32(&drain[x]), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -297,68 +304,70 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_wait_drain(smem_u32(&v_full[j % NST]), (j / NST) & 1);
       }
     }
-  } else if (warp < EW_WARP0) {
+  } else if (warp < Q_EW_WARP0) {
     if (lane == 0) {
       // ---------------------------------------------------------- UMMA issuers
-      // role 0: S = Q K^T and dQ += dS K; role 1: T = R K^T and dR += dT K;
-      // role 2: U = dO V^T. K-major operands for the scores, K MN-major for
-      // the gradients.
+      // role 0: S = Q K^T; role 1: T = R K^T; role 2: U = dO V^T (K-major
+      // operands); role 3: dQ += dS K and dR += dT K (K MN-major).
       const int role = warp - 1;
-      constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
-      constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, 1);
-      const uint64_t adesc =
-          smem_desc_sw128(smem_u32(smem + (role == 0 ? OFF_Q : role == 1 ? OFF_R : OFF_DO)), 16, 1024);
-      const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + (role == 2 ? OFF_V : OFF_K)), 16, 1024);
-      const uint64_t kmn0 = smem_desc_sw128(smem_u32(smem + OFF_K), HALF_KV, 1024);
-      const uint32_t dcol = tbase + (role == 0 ? COL_S : role == 1 ? COL_T : COL_U);
-      const uint32_t gcol = tbase + (role == 0 ? COL_GS : COL_GT);
-      const uint32_t acol = tbase + (role == 0 ? COL_ACC0 : COL_ACC1);
-      uint64_t *b_full = role == 2 ? v_full : k_full;
       bool ok = mbar_wait(smem_u32(q_full), 0, ab);
-      // The operand stage of tile j is normally loaded before S, T, U of tile
-      // j - 1 are free: wait for it first, so that only that hand-over
-      // stands before the issue.
-      auto operand_ready = [&](int j) -> bool {
-        return mbar_wait(smem_u32(&b_full[j % NST]), (j / NST) & 1, ab);
-      };
-      auto issue_score = [&](int j) -> bool {
-        const int st = j % NST;
-        tc_fence_after();
-        const uint64_t bd = bdesc0 + st * (TILE_KV >> 4);
+      if (role < 3) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, 0);
+        const uint64_t adesc =
+            smem_desc_sw128(smem_u32(smem + (role == 0 ? OFF_Q : role == 1 ? OFF_R : OFF_DO)), 16, 1024);
+        const uint64_t bdesc0 = smem_desc_sw128(smem_u32(smem + (role == 2 ? OFF_V : OFF_K)), 16, 1024);
+        const uint32_t dcol = tbase + (role == 0 ? COL_S : role == 1 ? COL_T : COL_U);
+        uint64_t *b_full = role == 2 ? v_full : k_full;
+        // The operand stage of tile j is normally loaded before S, T, U of
+        // tile j - 1 are free: wait for it first, so that only that
+        // hand-over stands before the issue.
+        auto operand_ready = [&](int j) -> bool {
+          return mbar_wait(smem_u32(&b_full[j % NST]), (j / NST) & 1, ab);
+        };
+        auto issue_score = [&](int j) {
+          const int st = j % NST;
+          tc_fence_after();
+          const uint64_t bd = bdesc0 + st * (TILE_KV >> 4);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma_ss(dcol, adesc + (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2,
-                  bd + (ks >> 2) * (HALF_KV >> 4) + (ks & 3) * 2, idesc_s, ks > 0);
-        umma_commit(smem_u32(stu_full));
-        if (role == 2) umma_commit(smem_u32(&v_empty[st]));
-        return true;
-      };
-      ok = ok && operand_ready(0) && issue_score(0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_ss(dcol, adesc + (ks >> 2) * (HALF_Q >> 4) + (ks & 3) * 2,
+                    bd + (ks >> 2) * (HALF_KV >> 4) + (ks & 3) * 2, idesc_s, ks > 0);
+          umma_commit(smem_u32(stu_full));
+          if (role == 2) umma_commit(smem_u32(&v_empty[st]));
+        };
+        if (ok && operand_ready(0)) issue_score(0);
+        for (int j = 0; ok && j + 1 < n; ++j) {
           // S, T, U of tile j are in registers once stu_free completes.
-          if (!operand_ready(j + 1) || !mbar_wait_spin(smem_u32(stu_free), j & 1, ab) ||
-              !issue_score(j + 1))
-            break;
+          if (!operand_ready(j + 1) || !mbar_wait_spin(smem_u32(stu_free), j & 1, ab)) break;
+          issue_score(j + 1);
         }
-        if (role == 2) continue;
-        if (!mbar_wait_spin(smem_u32(gs_full), j & 1, ab)) break;
-        tc_fence_after();
-        const int st = j % NST;
-        const uint64_t km = kmn0 + st * (TILE_KV >> 4);
+      } else {
+        constexpr uint32_t idesc_g = idesc_bf16_f32(BM, D, 1);
+        const uint64_t kmn0 = smem_desc_sw128(smem_u32(smem + OFF_K), HALF_KV, 1024);
+        for (int j = 0; ok && j < n; ++j) {
+          if (!mbar_wait_spin(smem_u32(gs_full), j & 1, ab)) break;
+          tc_fence_after();
+          const int st = j % NST;
+          const uint64_t km = kmn0 + st * (TILE_KV >> 4);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          umma_ts(acol, gcol + ks * 8, km + ks * (2048 >> 4), idesc_g, (j > 0 || ks > 0));
-        umma_commit(smem_u32(acc_done));
-        umma_commit(smem_u32(&k_empty[st]));
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ts(tbase + COL_ACC0, tbase + COL_GS + ks * 8, km + ks * (2048 >> 4), idesc_g,
+                    (j > 0 || ks > 0));
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks)
+            umma_ts(tbase + COL_ACC1, tbase + COL_GT + ks * 8, km + ks * (2048 >> 4), idesc_g,
+                    (j > 0 || ks > 0));
+          umma_commit(smem_u32(acc_done));
+          umma_commit(smem_u32(&k_empty[st]));
+        }
+        umma_commit(smem_u32(acc_full));
       }
-      if (role != 2) umma_commit(smem_u32(acc_full));
       umma_commit(smem_u32(&drain[role]));
       mbar_wait_drain(smem_u32(&drain[role]), 0);
     }
   } else {
     // ------------------------------------------------------------ elementwise
-    const int qw = warp & 3, hf = (warp - EW_WARP0) >> 2;
+    const int qw = warp & 3, hf = (warp - Q_EW_WARP0) >> 2;
     const int row = qw * 32 + lane, grow = q0 + row;
     const uint32_t tl = tbase + (static_cast<uint32_t>(qw * 32) << 16);
     float nl = -INFINITY, s1 = 1.f, aa = 0.f, nd = 0.f;
@@ -808,7 +817,7 @@ cudaError_t launch_prefill_bwd(const void *q, const void *k, const void *v, cons
   a.g0 = static_cast<__nv_bfloat16 *>(dq);
   a.g1 = static_cast<__nv_bfloat16 *>(dr);
   const int nq = (L + qk::BM - 1) / qk::BM * B * Hq;
-  bwd_dq_kernel<<<nq, THREADS, qk::SMEM_BYTES, stream>>>(mq, mr, mo, mk, mv, a);
+  bwd_dq_kernel<<<nq, qk::Q_THREADS, qk::SMEM_BYTES, stream>>>(mq, mr, mo, mk, mv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

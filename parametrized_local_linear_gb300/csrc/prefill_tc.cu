@@ -76,7 +76,11 @@ constexpr int OFF_R = 2 * HALF_Q;
 constexpr int OFF_K = 4 * HALF_Q;             // 65536
 constexpr int OFF_V = OFF_K + NST * TILE_KV;  // 131072
 constexpr int OFF_STAT = OFF_V + NST * TILE_KV;  // 196608: [2][3][BM] row statistics
-constexpr int OFF_BAR = OFF_STAT + 2 * 3 * BM * 4;
+// Output staging: per epilogue warp two 2 KB boxes (o and o^SA) of 32 rows x
+// 32 dims bf16, 64-byte rows with the 64-byte swizzle of the store map.
+constexpr int OFF_OST = OFF_STAT + 2 * 3 * BM * 4;  // 199680, a multiple of 1024
+constexpr int OST_BOX = 32 * 32 * 2;
+constexpr int OFF_BAR = OFF_OST + 4 * 2 * OST_BOX;
 constexpr int NBAR = 2 + 4 * NST + 2 + 4 + 2 + 4 + 1 + 2 + 4;
 constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
 constexpr int SM_WARP0 = 3;                   // first softmax warp
@@ -92,6 +96,7 @@ struct PrefillArgs {
   __nv_bfloat16 *o1;  // optional (training): o^SA = O1 / l per row, bf16
   float *sbar;        // optional (training): sigma / l per row
   int Hq, Hkv, L, B, nqt, nitems;
+  int full_rounds;  // nitems / gridDim.x
   int Lk, qoff;  // keys per head; absolute position of query row 0 (Lk - L)
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned *err;
@@ -101,12 +106,36 @@ struct Item {
   int q0, ntiles, zq, zk;
 };
 
-// k-th work item of this CTA: rounds of gridDim.x items, longest first,
-// dealt left-to-right in even rounds and right-to-left in odd ones.
+// k-th work item of this CTA. The items are dealt in rounds of gridDim.x,
+// longest first, left-to-right in even rounds and right-to-left in odd ones,
+// which evens out the CTAs' totals. A CTA then walks its own items starting
+// at round (blockIdx.x mod its item count) and wrapping around: its total is
+// unchanged, but the CTAs no longer reach item boundaries (Q and R loads from
+// HBM, output stores) all at the same moment, as they would with equal-length
+// items in every round.
+// The CTA's schedule {item count, starting round} lives in shared memory
+// after the barriers and the TMEM slot / abort flag words; thread 0 writes it
+// before the first __syncthreads.
+__device__ __forceinline__ int *sched_words() {
+  extern __shared__ uint8_t smem_raw[];
+  const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023);
+  return reinterpret_cast<int *>(base + OFF_BAR + NBAR * 8 + 8);
+}
+__device__ __forceinline__ void item_schedule(const PrefillArgs &a, int *sched) {
+  const int G = gridDim.x, c = static_cast<int>(blockIdx.x), full = a.full_rounds;
+  const int pos_last = (full & 1) ? G - 1 - c : c;
+  const int count = full + (pos_last < a.nitems - full * G ? 1 : 0);
+  sched[0] = count;
+  sched[1] = count > 0 ? c % count : 0;
+}
 __device__ __forceinline__ bool item_of(const PrefillArgs &a, int k, Item &it) {
-  const int G = gridDim.x;
-  const int pos = (k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int o = k * G + pos;
+  const int *sched = sched_words();
+  const int G = gridDim.x, c = static_cast<int>(blockIdx.x), count = sched[0];
+  if (k >= count) return false;
+  int kr = k + sched[1];
+  if (kr >= count) kr -= count;
+  const int pos = (kr & 1) ? G - 1 - c : c;
+  const int o = kr * G + pos;
   if (o >= a.nitems) return false;
   const int per_qt = a.Hq * a.B;
   const int qt = a.nqt - 1 - o / per_qt;
@@ -122,6 +151,7 @@ __device__ __forceinline__ bool item_of(const PrefillArgs &a, int k, Item &it) {
 __global__ void __launch_bounds__(THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_r,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_o1,
                       const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -167,6 +197,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(smem_u32(o_free), 4);
     for (int x = 0; x < 4; ++x) mbar_init(smem_u32(&drain[x]), 1);
     *abort_flag = 0;
+    item_schedule(a, sched_words());
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -255,7 +286,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           // leaves only the P hand-over between the softmax and the issue.
           // The first value UMMA of an item overwrites O: the previous item's
           // epilogue must have read it.
-          if (j == 0 && k > 0 && !mbar_wait(smem_u32(o_free), (k - 1) & 1, ab)) { ok = false; break; }
+          if (j == 0 && k > 0 && !mbar_wait_spin(smem_u32(o_free), (k - 1) & 1, ab)) { ok = false; break; }
           if (!mbar_wait(smem_u32(&v_full[st]), (gg / NST) & 1, ab)) { ok = false; break; }
           if (!mbar_wait_spin(smem_u32(&p_full[2 * x]), (gg >> 1) & 1, ab)) { ok = false; break; }
           tc_fence_after();
@@ -436,9 +467,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp >= EP_WARP0 && warp < EP_WARP0 + 4) {
     // ------------------------------------------------------------ epilogue
+    // Each warp owns 32 rows. Per 32-dim part it writes its 32 x 32 box of o
+    // (and of o^SA when asked) into its staging boxes and one lane stores
+    // them with TMA: whole lines to global memory instead of 16-byte pieces
+    // of 32 rows, which kept the warp's stores, and so the release of O,
+    // waiting on the memory pipeline.
     const int qw = warp & 3;
     const int row = qw * 32 + lane;
     const uint32_t tl = tbase + (static_cast<uint32_t>(qw * 32) << 16);
+    const uint32_t box_o = smem_u32(smem + OFF_OST + qw * 2 * OST_BOX), box_o1 = box_o + OST_BOX;
+    // Row `lane` of a box: 64 bytes, 16-byte chunk c at c ^ ((lane >> 1) & 3).
+    const uint32_t rbase = lane * 64, rsw = (lane >> 1) & 3;
     int g = 0;
     Item it;
     for (int k = 0; item_of(a, k, it); ++k) {
@@ -454,11 +493,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const float g1 = (1.f + sg * inv) * inv;
       // Correction (Sigma rho) = O2/l - (O1/l)(sigma/l); o = O1/l - correction.
       const float gc = sg * inv * inv;
-      const bool want_cor = a.cor != nullptr;
+      const bool want_cor = a.cor != nullptr, want_o1 = a.o1 != nullptr;
       const bool row_ok = grow < a.L &&
                           PLX_IN_BOUNDS(it.zq >= 0 && it.zq < a.B * a.Hq && grow >= 0, ab);
+      // The warp's box holds rows q0 + 32 qw ..; the store map drops rows >= L.
+      const bool box_live = it.q0 + qw * 32 < a.L;
       float csq = 0.f, osq = 0.f;
-      __nv_bfloat16 *orow = a.out + (static_cast<size_t>(it.zq) * a.L + grow) * D;
 #pragma unroll 1
       for (int part = 0; part < 4; ++part) {
         float o1[32], o2[32];
@@ -482,17 +522,28 @@ __global__ void __launch_bounds__(THREADS, 1)
             osq = fmaf(x0, x0, fmaf(x1, x1, osq));
           }
         }
-        if (row_ok) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + part * 32);
+        if (box_live) {
+          // The previous part's stores have read the staging boxes.
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
 #pragma unroll
-          for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          if (a.o1 != nullptr) {
+          for (int c = 0; c < 4; ++c)
+            st_shared_v4(box_o + rbase + ((c ^ rsw) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          if (want_o1) {
             // Saved for the backward pass: o^SA = O1 / l.
 #pragma unroll
             for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o1[e] * inv, o1[e + 1] * inv);
-            uint4 *d1 = reinterpret_cast<uint4 *>(a.o1 + (static_cast<size_t>(it.zq) * a.L + grow) * D + part * 32);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) d1[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            for (int c = 0; c < 4; ++c)
+              st_shared_v4(box_o1 + rbase + ((c ^ rsw) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                           pk[4 * c + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tm_o, box_o, part * 32, it.q0 + qw * 32, it.zq);
+            if (want_o1) tma_store_3d(&tm_o1, box_o1, part * 32, it.q0 + qw * 32, it.zq);
+            bulk_commit_group();
           }
         }
       }
@@ -502,6 +553,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (want_cor && row_ok)
         a.cor[static_cast<size_t>(it.zq) * a.L + grow] = osq > 0.f ? sqrtf(csq) / sqrtf(osq) : 0.f;
     }
+    // The staging boxes stay in use until the last stores have completed.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -513,6 +567,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 }  // namespace
+
+// Store map of a [heads][L][128] bf16 output: 32 x 32 boxes, 64-byte swizzle.
+static bool make_out_store_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, int L, int heads) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(heads)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(L) * D * 2};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool make_head_rows_map(EncodeTiledFn enc, CUtensorMap *map, const void *ptr, int L, int heads,
                         int box_rows) {
@@ -540,9 +607,11 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
   }
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return cudaErrorInvalidValue;
-  CUtensorMap mq, mr, mk, mv;
+  CUtensorMap mq, mr, mk, mv, mo, mo1;
   if (!make_head_rows_map(enc, &mq, q, L, B * Hq, BM) || !make_head_rows_map(enc, &mr, r, L, B * Hq, BM) ||
-      !make_head_rows_map(enc, &mk, k, Lk, B * Hkv, BN) || !make_head_rows_map(enc, &mv, v, Lk, B * Hkv, BN))
+      !make_head_rows_map(enc, &mk, k, Lk, B * Hkv, BN) || !make_head_rows_map(enc, &mv, v, Lk, B * Hkv, BN) ||
+      !make_out_store_map(enc, &mo, out, L, B * Hq) ||
+      !make_out_store_map(enc, &mo1, o1 != nullptr ? o1 : out, L, B * Hq))
     return cudaErrorInvalidValue;
   PrefillArgs a;
   a.out = static_cast<__nv_bfloat16 *>(out);
@@ -561,7 +630,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   a.err = err;
   const int grid = min(a.nitems, sm_count());
-  prefill_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mr, mk, mv, a);
+  a.full_rounds = a.nitems / grid;
+  prefill_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mr, mk, mv, mo, mo1, a);
   return cudaGetLastError();
 }
 
