@@ -13,12 +13,19 @@ the ragged long-context decode are timed after the steps (``extra``).
 ``--impl reference`` times the fp64 CPU oracle instead (the only other
 implementation of this method here), on a bounded row sample per step.
 
+``--config N`` (1-5: the fp32 tiny prefill, the 0.6B- and 1.7B-shaped
+prefills, the batched and the ragged decode) times that one workload alone and
+prints one line for it; ``--seed`` replaces the workload's input seed and
+``--nsplit`` fixes the decode's share count (0: the library's default). The
+prefill and decode launches of a timed step sit in NVTX ranges.
+
 Under torchrun each rank runs the same per-rank workload on its own GPU
 (weak scaling, no collective on the data path); rank 0 prints the line.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -382,6 +389,92 @@ def run_reference(args, world, rank):
     return 0
 
 
+CONFIGS = {1: inputs.TINY_PREFILL_F32, 2: inputs.PREFILL_0P6B, 3: inputs.PREFILL_1P7B,
+           4: inputs.DECODE_B64, 5: inputs.DECODE_RAGGED}
+
+
+def run_config(args, world, rank, local):
+    """Times one workload alone (one launch a step) and prints its JSON line.
+    A prefill reports algorithmic TFLOP/s (8 d flops per causal pair), a decode
+    algorithmic HBM GB/s; each rank runs the whole workload (replicas)."""
+    from parametrized_local_linear_gb300 import (build, plx_check_device_error, plx_decode_fwd,
+                                                 plx_prefill_fwd, plx_prefill_fwd_f32)
+    w = CONFIGS[args.config]
+    if args.seed is not None:
+        w = dataclasses.replace(w, seed=args.seed)
+    if rank == 0 or world == 1:
+        build.build()
+    barrier(world)
+    build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peaks_src = load_peaks()
+    cfg = {"workload": w.name, "seed": w.seed}
+    if isinstance(w, inputs.PrefillShape):
+        q, k, v, r = inputs.prefill_inputs_for(w, device=dev)
+        out = torch.empty_like(q)
+        f32 = w.dtype == torch.float32
+        call = plx_prefill_fwd_f32 if f32 else plx_prefill_fwd
+        fn = lambda: call(q, k, v, r, out)  # noqa: E731
+        units, scale, unit, tag = w.flops, 1e12, "TFLOP/s", "prefill"
+        kernel = "prefill_f32_kernel" if f32 else "prefill_tc_kernel"
+        roof = None if f32 else ("tensor", _peak(peaks, "bf16_tflops"), f"bf16_tflops ({peaks_src})")
+        dtype = "f32" if f32 else "bf16"
+    else:
+        dq, dr, kc, vc, sl = inputs.decode_inputs_for(w, device=dev)
+        lens = sl
+        sl = sl.to(dev)
+        out = torch.empty_like(dq)
+        fn = lambda: plx_decode_fwd(dq, dr, kc, vc, sl, out, nsplit=args.nsplit)  # noqa: E731
+        units, scale, unit, tag = w.bytes_moved(lens), 1e9, "GB/s", "decode"
+        kernel = "decode_split_kernel + combine"
+        roof = ("hbm", _peak(peaks, "hbm_gbs"), f"hbm_gbs ({peaks_src})")
+        dtype = "bf16"
+        cfg["nsplit"] = args.nsplit
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    plx_check_device_error()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_end = time.time() + 0.6
+        while time.time() < t_end:
+            fn()
+            torch.cuda.synchronize(dev)
+        for e0, e1 in evs:
+            torch.cuda.nvtx.range_push(tag)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    plx_check_device_error()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    ms_max = max_over_ranks(ms, world, dev)
+    K = args.steps
+    value = whole_job_rate(world, units, K, ms_max) / scale
+    per_launch = units / (ms / K * 1e-3) / scale
+    line = {"metric": f"{w.name} {tag} {unit}", "value": value, "unit": unit, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": dict(cfg, l2="inputs fit in L2 (tiny workload)"
+                           if w.name == inputs.TINY_PREFILL_F32.name else "inputs larger than L2"),
+            "clocks": clk.summary(), "gpu_launches": K * (2 if tag == "decode" else 1)}
+    if roof is not None:
+        bound, peak, src = roof
+        line["roofline"] = {"bound": bound, "kernel": kernel, "achieved": per_launch, "peak": peak,
+                            "unit": unit, "frac": per_launch / peak, "peak_source": src,
+                            "traffic": None}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ncu_case(case):
     """Profiling-sized cases for ncu (one kernel, few launches, inputs > L2)."""
     from parametrized_local_linear_gb300 import (build, plx_check_device_error, plx_decode_fwd,
@@ -439,6 +532,12 @@ def main():
                     help="under torchrun, deal one batch's (sequence, kv head) units among the "
                          "ranks (strong scaling) instead of a full replica per rank")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--config", type=int, choices=sorted(CONFIGS), default=None,
+                    help="time one workload alone: 1 fp32 tiny prefill, 2 0.6B-shaped prefill, "
+                         "3 1.7B-shaped prefill, 4 batched decode, 5 ragged decode")
+    ap.add_argument("--seed", type=int, default=None, help="input seed for --config")
+    ap.add_argument("--nsplit", type=int, default=0,
+                    help="decode share count for --config 4/5 (0: the library's default)")
     ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_ragged", "decode_long", "backward",
                                            "projection"], default=None,
                     help="run 3 warm-up + 3 launches of one kernel on a profiling-sized case "
@@ -451,6 +550,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.config is not None:
+        return run_config(args, world, rank, local)
 
     from parametrized_local_linear_gb300 import (build, plx_check_device_error, plx_decode_fwd,
                                                  plx_prefill_fwd)
@@ -496,6 +597,7 @@ def main():
     dviews = (dq[b0:b1], dr[b0:b1], kc[tok0:tok1], vc[tok0:tok1], sl[b0:b1], dout[b0:b1])
 
     def step(ev):
+        torch.cuda.nvtx.range_push("prefill")
         ev[0].record(stream)
         if args.shard:
             for c in pcalls:
@@ -503,9 +605,12 @@ def main():
         else:
             plx_prefill_fwd(q, k, v, r, out, lse)
         ev[1].record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.nvtx.range_push("decode")
         if b1 > b0:
             plx_decode_fwd(*dviews)
         ev[2].record(stream)
+        torch.cuda.nvtx.range_pop()
 
     for _ in range(args.warmup):
         step([torch.cuda.Event(enable_timing=True) for _ in range(3)])

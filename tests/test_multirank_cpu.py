@@ -133,3 +133,13 @@ def test_decode_shards_partition_the_sequences(world):
     # A uniform batch splits evenly whenever the world size divides it.
     assert [bench.decode_shard([8192] * 64, 8, r) for r in range(8)] == \
         [(8 * r, 8 * r + 8) for r in range(8)]
+
+
+def test_config_selection_covers_the_five_workloads():
+    """--config 1..5 names each of the five workloads once, and --seed gives
+    the same shape with another seed."""
+    import dataclasses
+    assert sorted(bench.CONFIGS) == [1, 2, 3, 4, 5]
+    assert sorted(w.name for w in bench.CONFIGS.values()) == sorted(inputs.WORKLOADS)
+    w = dataclasses.replace(bench.CONFIGS[4], seed=7)
+    assert w.seed == 7 and w.B == inputs.DECODE_B64.B and w.name == inputs.DECODE_B64.name
