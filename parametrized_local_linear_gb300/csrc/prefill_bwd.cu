@@ -32,13 +32,15 @@
 // Neither kernel needs atomics: each output row is owned by one CTA. The
 // elementwise warps release S, T and U as soon as they have loaded them
 // (stu_free), so the next tile's score UMMAs run under the elementwise work
-// and the current tile's gradient UMMAs. 12 warps: 0 TMA producer; 1, 2, 3
-// one UMMA-issuing thread each (warp 1 also allocates TMEM); 4..11
-// elementwise (two warps per TMEM lane quarter, each taking half of the
-// tile's 64 columns; there is no row reduction, so the columns split
-// freely). The UMMAs are spread over three threads because one thread
-// cannot issue tcgen05.mma as fast as the tensor core retires these shapes
-// (measured 50-100 cycles per issue under load against 48-64 cycles of work).
+// and the current tile's gradient UMMAs. The key-block kernel has 12 warps:
+// 0 TMA producer; 1, 2, 3 one UMMA-issuing thread each (warp 1 also
+// allocates TMEM); 4..11 elementwise (two warps per TMEM lane quarter, each
+// taking half of the tile's 64 columns; there is no row reduction, so the
+// columns split freely). The query-block kernel has a fourth issuing thread
+// (warp 4) for its gradient products and elementwise warps 5..12. The UMMAs
+// are spread over several threads because one thread cannot issue
+// tcgen05.mma as fast as the tensor core retires these shapes (measured
+// 50-100 cycles per issue under load against 48-64 cycles of work).
 #include <math.h>
 
 #include <type_traits>
