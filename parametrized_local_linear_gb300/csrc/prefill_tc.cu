@@ -96,7 +96,6 @@ struct PrefillArgs {
   __nv_bfloat16 *o1;  // optional (training): o^SA = O1 / l per row, bf16
   float *sbar;        // optional (training): sigma / l per row
   int Hq, Hkv, L, B, nqt, nitems;
-  int full_rounds;  // nitems / gridDim.x
   int Lk, qoff;  // keys per head; absolute position of query row 0 (Lk - L)
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned *err;
@@ -106,36 +105,14 @@ struct Item {
   int q0, ntiles, zq, zk;
 };
 
-// k-th work item of this CTA. The items are dealt in rounds of gridDim.x,
-// longest first, left-to-right in even rounds and right-to-left in odd ones,
-// which evens out the CTAs' totals. A CTA then walks its own items starting
-// at round (blockIdx.x mod its item count) and wrapping around: its total is
-// unchanged, but the CTAs no longer reach item boundaries (Q and R loads from
-// HBM, output stores) all at the same moment, as they would with equal-length
-// items in every round.
-// The CTA's schedule {item count, starting round} lives in shared memory
-// after the barriers and the TMEM slot / abort flag words; thread 0 writes it
-// before the first __syncthreads.
-__device__ __forceinline__ int *sched_words() {
-  extern __shared__ uint8_t smem_raw[];
-  const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023);
-  return reinterpret_cast<int *>(base + OFF_BAR + NBAR * 8 + 8);
-}
-__device__ __forceinline__ void item_schedule(const PrefillArgs &a, int *sched) {
-  const int G = gridDim.x, c = static_cast<int>(blockIdx.x), full = a.full_rounds;
-  const int pos_last = (full & 1) ? G - 1 - c : c;
-  const int count = full + (pos_last < a.nitems - full * G ? 1 : 0);
-  sched[0] = count;
-  sched[1] = count > 0 ? c % count : 0;
-}
+// k-th work item of this CTA: rounds of gridDim.x items, longest first,
+// dealt left-to-right in even rounds and right-to-left in odd ones. All CTAs
+// work on the same round at about the same time, so the K/V tiles the round's
+// items stream stay in L2 between the CTAs that read them.
 __device__ __forceinline__ bool item_of(const PrefillArgs &a, int k, Item &it) {
-  const int *sched = sched_words();
-  const int G = gridDim.x, c = static_cast<int>(blockIdx.x), count = sched[0];
-  if (k >= count) return false;
-  int kr = k + sched[1];
-  if (kr >= count) kr -= count;
-  const int pos = (kr & 1) ? G - 1 - c : c;
-  const int o = kr * G + pos;
+  const int G = gridDim.x;
+  const int pos = (k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int o = k * G + pos;
   if (o >= a.nitems) return false;
   const int per_qt = a.Hq * a.B;
   const int qt = a.nqt - 1 - o / per_qt;
@@ -197,7 +174,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(smem_u32(o_free), 4);
     for (int x = 0; x < 4; ++x) mbar_init(smem_u32(&drain[x]), 1);
     *abort_flag = 0;
-    item_schedule(a, sched_words());
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -630,7 +606,6 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   a.err = err;
   const int grid = min(a.nitems, sm_count());
-  a.full_rounds = a.nitems / grid;
   prefill_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mr, mk, mv, mo, mo1, a);
   return cudaGetLastError();
 }
