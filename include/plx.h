@@ -197,11 +197,11 @@ plx_status plx_decode_fwd(const void *q, const void *r, const void *kcache, cons
  * the W keys of the batch, sequence-major, then kv head, then token; at most
  * W shares take part), and a caller-provided device workspace of at least
  * plx_decode_workspace_bytes(B, Hq, Hkv, d, nsplit) bytes, 16-byte aligned.
- * nsplit <= 0 picks the default schedule: plx_decode_default_nsplit shares,
- * fewer for small batches so that every share holds at least 512 keys; when
- * all sequences of nonzero length have one length, a count that cuts every
- * (sequence, kv head) row at the same keys or gives every share whole rows,
- * if that keeps at least 80% of the shares.
+ * nsplit <= 0 picks the default schedule: floor(sqrt(W)) shares, at most
+ * plx_decode_default_nsplit (small batches get fewer, shorter shares); when
+ * all sequences of nonzero length have one length, at most 256, lowered to a
+ * count that cuts every (sequence, kv head) row at the same keys or gives
+ * every share whole rows, if that keeps at least 80% of the shares.
  * workspace == NULL allocates as plx_decode_fwd does. The result does not
  * depend on nsplit beyond fp32 rounding.
  */

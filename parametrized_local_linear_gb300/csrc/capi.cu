@@ -296,8 +296,8 @@ int plx_decode_default_nsplit(int B, int Hkv) {
   // One wave of the split kernel: two CTAs fit on an SM (its registers), and
   // every CTA takes an equal share of the batch's keys, so a single wave keeps
   // every SM streaming until the end with no tail. Lengths live on the
-  // device, so the kernel itself lowers the count for small batches (at least
-  // 512 keys a CTA). Measured on GB300 with per-sequence splits before this
+  // device, so the kernel itself lowers the count for small batches
+  // (floor(sqrt(W)) CTAs for W keys). Measured on GB300 with per-sequence splits before this
   // schedule: uniform batches ran fastest at 256 CTAs (B = 1..32, 8192
   // tokens), a ragged one (B = 8, 16k-131k tokens) needed 32 splits a
   // sequence to even out its lengths.

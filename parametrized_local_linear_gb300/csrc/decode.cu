@@ -66,19 +66,24 @@ static_assert(OFF_BAR % 8 == 0 && OFF_PLAN % 16 == 0, "barrier and plan alignmen
 constexpr int SMEM_BYTES = OFF_PLAN + 64 + 1024;  // + alignment slack
 constexpr int REC = 2 * D + 2;                // floats per partial record
 constexpr int THREADS = 32 * (NCW + 1);
-// Fewest keys the default schedule gives one CTA: below about 512 keys the
-// fixed cost of a CTA (tensor-map prefetch, pipeline fill, the merge) is no
-// longer small against its stream, and small batches ran fastest on GB300
-// with 128 to 256 CTAs of 256 to 1024 keys each.
-constexpr int kDefaultMinKeys = 512;
+// The default schedule takes floor(sqrt(W)) CTAs for W keys (at most the
+// grid): a small call's time is a fixed cost plus its longest share's
+// stream, and on GB300 the fastest CTA counts (L2 flushed before each call)
+// were 64 for 4096 keys (14.7 us against 20.7 with 8 CTAs of 512 keys), 128
+// for 16384 (16.7 against 22.5) and 192 to 256 for 65536 (22.5 against 23.6
+// with 128). For a batch of one length (whose shares are then aligned with
+// the rows) at most kUniformMaxShares: from there on 256 CTAs beat the full
+// grid of 304 by 1-6% (B = 2 x 8192: 24.8 against 26.2 us); a ragged batch ran
+// 0.9% faster on the full grid.
+constexpr long long kUniformMaxShares = 256;
 
 struct DecodeArgs {
   const __nv_bfloat16 *q, *r;
   const int *seqlens;
   float *recs;  // [(nshare * G + B * Hq)][REC] partial records
   int2 *meta;   // [B * Hkv] {first record slot, number of slots} of each (sequence, kv head)
-  int B, Hq, Hkv, G, nshare, min_keys;
-  bool align;        // default schedule: align the shares with the rows of a uniform batch
+  int B, Hq, Hkv, G, nshare;
+  bool dflt;         // default schedule: floor(sqrt(W)) shares; for a uniform batch at most 256, aligned with the rows
   float scale_log2;  // log2(e) / sqrt(d)
   unsigned *err;
 };
@@ -180,9 +185,15 @@ __global__ void __launch_bounds__(THREADS)
       nz = 0;
     }
     const long long W = T * a.Hkv;
-    long long n = (W + a.min_keys - 1) / a.min_keys;
+    long long n = W;
+    if (a.dflt) {
+      n = static_cast<long long>(sqrtf(static_cast<float>(W)));
+      while (n > 0 && n * n > W) --n;
+      while ((n + 1) * (n + 1) <= W) ++n;
+      if (nz > 0 && lmin == lmax) n = min(n, kUniformMaxShares);
+    }
     n = max(1LL, min(static_cast<long long>(a.nshare), n));
-    if (a.align && nz > 0 && lmin == lmax) {
+    if (a.dflt && nz > 0 && lmin == lmax) {
       // Rows of one length: cut every row at the same keys (k shares a row)
       // or give every share whole rows (m rows a share), so that the CTAs
       // streaming the kv heads of a sequence read the same tokens at the
@@ -633,8 +644,7 @@ cudaError_t launch_decode(const void *q, const void *r, const void *kcache, cons
   a.Hkv = Hkv;
   a.G = Hq / Hkv;
   a.nshare = nshare;
-  a.min_keys = default_share ? kDefaultMinKeys : 1;
-  a.align = default_share;
+  a.dflt = default_share;
   a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   a.err = err;
   decode_split_kernel<<<nshare, THREADS, SMEM_BYTES, stream>>>(mk, mv, a);

@@ -8,17 +8,27 @@ The CUDA split kernel computes the same integer formulas on the device (its
 parity against the oracle is in test_decode_gpu.py); this test pins the
 formulas themselves.
 """
+import math
 import random
 
 import pytest
 
 
-def share_count(lens, Hkv, nshare, min_keys, align):
+def share_count(lens, Hkv, nshare, default):
+    """Explicit counts take min(nshare, W) shares; the default schedule takes
+    floor(sqrt(W)) (at most nshare), and for a batch whose nonzero lengths
+    are all equal at most 256, aligned with its rows."""
     lens = [max(x, 0) for x in lens]
     W = sum(lens) * Hkv
-    n = max(1, min(nshare, -(-W // min_keys)))
     nz = [x for x in lens if x > 0]
-    if align and nz and min(nz) == max(nz):
+    uniform = bool(nz) and min(nz) == max(nz)
+    n = W
+    if default:
+        n = math.isqrt(W)
+        if uniform:
+            n = min(n, 256)
+    n = max(1, min(nshare, n))
+    if default and uniform:
         R, floor_n, best = len(nz) * Hkv, (4 * n + 4) // 5, 0
         if R <= n:
             best = R * (n // R)
@@ -97,7 +107,7 @@ def test_random_batches_explicit_share_counts(seed):
         Hkv = rng.choice([1, 2, 3, 8])
         if sum(lens) == 0:
             continue
-        n = share_count(lens, Hkv, rng.choice([1, 2, 3, 7, 64, 304]), 1, False)
+        n = share_count(lens, Hkv, rng.choice([1, 2, 3, 7, 64, 304]), False)
         check(lens, Hkv, n)
 
 
@@ -113,10 +123,10 @@ def test_random_batches_default_schedule(seed):
         Hkv = rng.choice([1, 2, 8])
         if sum(lens) == 0:
             continue
-        n = share_count(lens, Hkv, 304, 512, True)
+        n = share_count(lens, Hkv, 304, True)
         W = sum(lens) * Hkv
         assert 1 <= n <= 304
-        assert n <= max(1, -(-W // 512))  # no share below 512 keys unless there is one share
+        assert n <= max(1, math.isqrt(W))  # the alignment never raises the count
         check(lens, Hkv, n)
 
 
@@ -125,12 +135,15 @@ def test_random_batches_default_schedule(seed):
     ([8192] * 128, 8, 256),      # 1024 rows: four a share
     ([8192] * 32, 8, 256),       # 256 rows: one a share
     ([32768] * 16, 8, 256),      # 128 rows cut in two
-    ([8192] * 4, 8, 288),        # 32 rows cut in nine
-    ([8192], 8, 128),            # 512 keys a share at least
-    ([131072], 8, 304),          # 8 rows cut in 38
-    ([40] * 64, 8, 32),          # 512 short rows, 16 a share
-    ([0, 100, 100, 0, 100], 2, 2),
-    ([16384, 131072, 50000], 8, 304),  # ragged: no alignment, two CTAs per SM
+    ([8192] * 4, 8, 256),        # 32 rows cut in eight
+    ([8192] * 2, 8, 256),        # 16 rows cut in sixteen
+    ([8192], 8, 256),            # sqrt(65536) = 256 shares: 8 rows cut in 32
+    ([512], 8, 64),              # sqrt(4096) = 64: 8 rows cut in 8
+    ([2048], 8, 128),            # sqrt(16384) = 128: 8 rows cut in 16
+    ([131072], 8, 256),          # 8 rows cut in 32
+    ([40] * 64, 8, 128),         # 512 short rows: sqrt(20480) = 143, whole rows, 4 a share
+    ([0, 100, 100, 0, 100], 2, 24),  # sqrt(600) = 24: 6 rows cut in 4
+    ([16384, 131072, 50000], 8, 304),  # ragged: no cap, no alignment
 ])
 def test_default_share_counts(lens, Hkv, want):
-    assert share_count(lens, Hkv, 304, 512, True) == want
+    assert share_count(lens, Hkv, 304, True) == want
