@@ -854,8 +854,8 @@ def main():
             tflops(f"prefill_sweep_B{B_}_L{L_}", fl,
                    launch_s(lambda: plx_prefill_fwd(qs, ks, vs, rs, os_), 5))
             del qs, ks, vs, rs, os_
-        for B_, ctx in ((1, 8192), (1, 131072), (4, 8192), (8, 8192), (32, 8192), (128, 8192),
-                        (16, 2048), (16, 32768)):
+        for B_, ctx in ((1, 512), (1, 2048), (1, 8192), (1, 131072), (4, 8192), (8, 8192),
+                        (32, 8192), (128, 8192), (16, 2048), (16, 32768)):
             ds = inputs.decode_inputs(B_, 16, 8, 128, [ctx] * B_, torch.bfloat16, 0.05, 3000 + B_,
                                       device=dev)
             sls = ds[4].to(dev)
