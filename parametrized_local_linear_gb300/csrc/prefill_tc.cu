@@ -58,6 +58,8 @@
 // rarely touches O in TMEM.
 #include <math.h>
 
+#include <type_traits>
+
 #include "plx_device.cuh"
 #include "plx_internal.h"
 
@@ -475,54 +477,63 @@ __global__ void __launch_bounds__(THREADS, 1)
       // The warp's box holds rows q0 + 32 qw ..; the store map drops rows >= L.
       const bool box_live = it.q0 + qw * 32 < a.L;
       float csq = 0.f, osq = 0.f;
+      // The optional outputs are compile-time choices of the part loop, so
+      // its unrolled element loop carries no branch.
+      auto drain = [&](auto cor_tag, auto o1_tag) {
+        constexpr bool COR = decltype(cor_tag)::value, O1 = decltype(o1_tag)::value;
 #pragma unroll 1
-      for (int part = 0; part < 4; ++part) {
-        float o1[32], o2[32];
-        tmem_ld32(tl + COL_O1 + part * 32, o1);
-        tmem_ld32(tl + COL_O2 + part * 32, o2);
-        tmem_wait_ld();
-        if (part == 3) {
-          // O has been read: the next item's value UMMAs may overwrite it.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(o_free));
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float x0 = fmaf(o1[e], g1, -o2[e] * inv), x1 = fmaf(o1[e + 1], g1, -o2[e + 1] * inv);
-          pk[e >> 1] = pack_bf16x2(x0, x1);
-          if (want_cor) {
-            const float c0 = fmaf(-o1[e], gc, o2[e] * inv), c1 = fmaf(-o1[e + 1], gc, o2[e + 1] * inv);
-            csq = fmaf(c0, c0, fmaf(c1, c1, csq));
-            osq = fmaf(x0, x0, fmaf(x1, x1, osq));
+        for (int part = 0; part < 4; ++part) {
+          float o1[32], o2[32];
+          tmem_ld32(tl + COL_O1 + part * 32, o1);
+          tmem_ld32(tl + COL_O2 + part * 32, o2);
+          tmem_wait_ld();
+          if (part == 3) {
+            // O has been read: the next item's value UMMAs may overwrite it.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(o_free));
           }
-        }
-        if (box_live) {
-          // The previous part's stores have read the staging boxes.
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            st_shared_v4(box_o + rbase + ((c ^ rsw) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          if (want_o1) {
-            // Saved for the backward pass: o^SA = O1 / l.
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o1[e] * inv, o1[e + 1] * inv);
+          for (int e = 0; e < 32; e += 2) {
+            const float x0 = fmaf(o1[e], g1, -o2[e] * inv), x1 = fmaf(o1[e + 1], g1, -o2[e + 1] * inv);
+            pk[e >> 1] = pack_bf16x2(x0, x1);
+            if (COR) {
+              const float c0 = fmaf(-o1[e], gc, o2[e] * inv), c1 = fmaf(-o1[e + 1], gc, o2[e + 1] * inv);
+              csq = fmaf(c0, c0, fmaf(c1, c1, csq));
+              osq = fmaf(x0, x0, fmaf(x1, x1, osq));
+            }
+          }
+          if (box_live) {
+            // The previous part's stores have read the staging boxes.
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-              st_shared_v4(box_o1 + rbase + ((c ^ rsw) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                           pk[4 * c + 3]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tm_o, box_o, part * 32, it.q0 + qw * 32, it.zq);
-            if (want_o1) tma_store_3d(&tm_o1, box_o1, part * 32, it.q0 + qw * 32, it.zq);
-            bulk_commit_group();
+              st_shared_v4(box_o + rbase + ((c ^ rsw) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            if (O1) {
+              // Saved for the backward pass: o^SA = O1 / l.
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16x2(o1[e] * inv, o1[e + 1] * inv);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                st_shared_v4(box_o1 + rbase + ((c ^ rsw) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                             pk[4 * c + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tm_o, box_o, part * 32, it.q0 + qw * 32, it.zq);
+              if (O1) tma_store_3d(&tm_o1, box_o1, part * 32, it.q0 + qw * 32, it.zq);
+              bulk_commit_group();
+            }
           }
         }
-      }
+      };
+      if (want_cor && want_o1) drain(std::true_type{}, std::true_type{});
+      else if (want_cor) drain(std::true_type{}, std::false_type{});
+      else if (want_o1) drain(std::false_type{}, std::true_type{});
+      else drain(std::false_type{}, std::false_type{});
       if (a.lse != nullptr && row_ok)
         a.lse[static_cast<size_t>(it.zq) * a.L + grow] = (m_used + log2f(l)) * 0.6931471805599453f;
       if (a.sbar != nullptr && row_ok) a.sbar[static_cast<size_t>(it.zq) * a.L + grow] = sg * inv;
