@@ -54,6 +54,8 @@ def test_train_forward_saves_osa_and_sbar():
     (2, 4, 2, 130),    # GQA pairs, just over one 128-row block
     (1, 2, 2, 64),     # one key tile, no GQA
     (1, 4, 1, 257),    # a group of 4 query heads per kv head; 1-row tail
+    (1, 8, 1, 150),    # a group of 8: the key-block kernel walks 8 heads
+    (1, 16, 1, 70),    # one kv head for 16 query heads (MQA)
 ])
 def test_backward_matches_oracle(B, Hq, Hkv, L):
     q, k, v, r, do = _case(B, Hq, Hkv, L, 50 + L)

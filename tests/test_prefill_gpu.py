@@ -49,6 +49,8 @@ def test_f32_shapes_match_oracle(B, Hq, Hkv, L, d):
     (1, 1, 1, 64),     # exactly one key tile
     (1, 2, 1, 129),    # one row into the second query tile
     (1, 4, 1, 383),    # GQA group of 4, three query tiles, ragged
+    (1, 8, 1, 300),    # GQA group of 8
+    (1, 16, 1, 130),   # one kv head for 16 query heads (MQA), one-row tail
 ])
 def test_bf16_small_matches_oracle_every_row(B, Hq, Hkv, L):
     q, k, v, r = inputs.prefill_inputs(B, Hq, Hkv, L, 128, torch.bfloat16, 0.05, 7 + L)
