@@ -448,16 +448,10 @@ __device__ __forceinline__ uint64_t f2(float lo, float hi) {
   return r;
 }
 __device__ __forceinline__ float f2lo(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  (void)hi;
-  return lo;
+  return __uint_as_float(static_cast<uint32_t>(v));
 }
 __device__ __forceinline__ float f2hi(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  (void)lo;
-  return hi;
+  return __uint_as_float(static_cast<uint32_t>(v >> 32));
 }
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t r;
